@@ -1,0 +1,204 @@
+"""ctypes + numpy wrapper around gptq_oracle.c (test infrastructure only).
+
+Arrays cross as numpy buffers: int32 words, uint16 bit patterns of fp16/bf16
+values, float32 / float64 results.  Torch tensors are accepted and converted on
+the CPU; nothing here touches a GPU.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gptq_oracle.c")
+_LIBDIR = os.path.join(_HERE, "lib")
+_SO = os.path.join(_LIBDIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DT = {"fp16": 0, "bf16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile gptq_oracle.c into oracle/lib/liboracle.so (OpenMP when available)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+    tmp = _SO + f".tmp{os.getpid()}"
+    try:
+        subprocess.run(base + ["-fopenmp", "-o", tmp, _SRC], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + ["-o", tmp, _SRC], check=True, capture_output=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            P = C.c_void_p
+            I = C.c_int
+            sigs = {
+                "oracle_unpack_codes": [P, I, I, I, P],
+                "oracle_pack_codes": [P, I, I, I, P],
+                "oracle_unpack_zeros": [P, I, I, I, P],
+                "oracle_pack_zeros": [P, I, I, I, P],
+                "oracle_num_groups": [I, I],
+                "oracle_dequant": [P, P, P, I, P, I, I, I, I, P],
+                "oracle_linear": [P, P, P, I, P, I, I, I, I, P, I, P, I, P, I, P],
+                "oracle_check_rules": [I, I, I, I, I, I, I, I, P, I],
+                "oracle_runtime_dims": [P, I, I, I, P, P],
+                "oracle_runtime_layout": [P, P, P, P, I, I, I, I, P, P, P, P, P],
+                "oracle_num_threads": [],
+            }
+            for name, args in sigs.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = I
+            L.oracle_half_to_float.argtypes = [C.c_uint16, I]
+            L.oracle_half_to_float.restype = C.c_float
+            _lib = L
+    return _lib
+
+
+def _np(a, dtype):
+    """torch tensor or array -> contiguous numpy array viewed as dtype (bit patterns kept)."""
+    if a is None:
+        return None
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype in (torch.float16, torch.bfloat16):
+                a = a.view(torch.int16)
+            a = a.numpy()
+    except ImportError:
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype.itemsize == np.dtype(dtype).itemsize and a.dtype != np.dtype(dtype):
+        a = a.view(dtype)
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle: {what} rejected its arguments")
+
+
+def num_groups(K: int, group_size: int) -> int:
+    return lib().oracle_num_groups(K, group_size)
+
+
+def unpack_codes(qweight, bits: int) -> np.ndarray:
+    qw = _np(qweight, np.int32)
+    K, N = qw.shape[0] * 32 // bits, qw.shape[1]
+    out = np.empty((K, N), np.uint8)
+    _check(lib().oracle_unpack_codes(_p(qw), K, N, bits, _p(out)), "unpack_codes")
+    return out
+
+
+def pack_codes(codes, bits: int) -> np.ndarray:
+    c = _np(codes, np.uint8)
+    K, N = c.shape
+    out = np.empty((K * bits // 32, N), np.int32)
+    _check(lib().oracle_pack_codes(_p(c), K, N, bits, _p(out)), "pack_codes")
+    return out
+
+
+def unpack_zeros(qzeros, N: int, bits: int) -> np.ndarray:
+    qz = _np(qzeros, np.int32)
+    G = qz.shape[0]
+    out = np.empty((G, N), np.int32)
+    _check(lib().oracle_unpack_zeros(_p(qz), G, N, bits, _p(out)), "unpack_zeros")
+    return out
+
+
+def pack_zeros(z, bits: int) -> np.ndarray:
+    zz = _np(z, np.int32)
+    G, N = zz.shape
+    out = np.empty((G, N * bits // 32), np.int32)
+    _check(lib().oracle_pack_zeros(_p(zz), G, N, bits, _p(out)), "pack_zeros")
+    return out
+
+
+def dequant(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: str) -> np.ndarray:
+    """Dense W float32 [N, K]."""
+    qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
+    sc, gi = _np(scales, np.uint16), _np(g_idx, np.int32)
+    K, N = qw.shape[0] * 32 // bits, qw.shape[1]
+    W = np.empty((N, K), np.float32)
+    _check(lib().oracle_dequant(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size, _p(W)),
+           "dequant")
+    return W
+
+
+def linear(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: str, x,
+           rows=None, cols=None) -> np.ndarray:
+    """y[rows][cols] = x[rows] . W[cols]^T in float64 (all rows / columns by default)."""
+    qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
+    sc, gi = _np(scales, np.uint16), _np(g_idx, np.int32)
+    xx = _np(x, np.uint16)
+    K, N = qw.shape[0] * 32 // bits, qw.shape[1]
+    M = xx.shape[0]
+    assert xx.shape[1] == K
+    r = np.arange(M, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, np.int32)
+    y = np.empty((len(r), len(c)), np.float64)
+    _check(lib().oracle_linear(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size,
+                               _p(xx), M, _p(r), len(r), _p(c), len(c), _p(y)), "linear")
+    return y
+
+
+def check_rules(bits, qweight_shape, qzeros_shape, scales_shape, in_features, g_idx=None) -> int:
+    gi = _np(g_idx, np.int32)
+    n = 0 if gi is None else gi.shape[0]
+    return lib().oracle_check_rules(bits, qweight_shape[0], qweight_shape[1], qzeros_shape[0],
+                                    qzeros_shape[1], scales_shape[0], scales_shape[1], in_features,
+                                    _p(gi), n)
+
+
+def runtime_dims(g_idx, K: int, N: int, group_size: int) -> tuple[int, int]:
+    gi = _np(g_idx, np.int32)
+    kr, npad = C.c_int(), C.c_int()
+    _check(lib().oracle_runtime_dims(_p(gi), K, N, group_size, C.byref(kr), C.byref(npad)), "runtime_dims")
+    return kr.value, npad.value
+
+
+def runtime_layout(qweight, qzeros, scales, g_idx, bits: int, group_size: int) -> dict:
+    """Expected contents of a runtime handle: wr bytes, perm, cgid, s_r (uint16 bits), z_r."""
+    qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
+    sc, gi = _np(scales, np.uint16), _np(g_idx, np.int32)
+    K, N = qw.shape[0] * 32 // bits, qw.shape[1]
+    G = num_groups(K, group_size)
+    Kr, Np = runtime_dims(gi, K, N, group_size)
+    out = dict(
+        Kr=Kr, Np=Np, G=G,
+        wr=np.empty(Kr // 128 * bits * Np * 16, np.uint8),
+        perm=np.empty(Kr, np.int32),
+        cgid=np.empty(Kr // 32, np.int32),
+        s_r=np.empty((G, Np), np.uint16),
+        z_r=np.empty((G, Np), np.uint8),
+    )
+    _check(lib().oracle_runtime_layout(_p(qw), _p(qz), _p(sc), _p(gi), K, N, bits, group_size,
+                                       _p(out["wr"]), _p(out["perm"]), _p(out["cgid"]),
+                                       _p(out["s_r"]), _p(out["z_r"])), "runtime_layout")
+    return out
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+def half_to_float(bits_u16: int, dtype: str) -> float:
+    return lib().oracle_half_to_float(bits_u16, DT[dtype])
