@@ -1,0 +1,177 @@
+/*
+ * gptq.h - C ABI of the GB300 (sm_103a) GPTQ weight-only linear layer.
+ *
+ *     y[M, N] = x[M, K] . W^T,   W[n, k] = (code[k, n] - zero[g, n]) * scale[g, n],  g = g_idx[k]
+ *
+ * The operation and the checkpoint layout it consumes are the ones of
+ *   - tensref.org "GPTQ packed checkpoint" (sections GptqLayer, QuantizeConfig, Reader and
+ *     "Reject the file when": rules GPTQ-001 .. GPTQ-006), and
+ *   - inference.shantanugoel.com ch. 39 "Quantized checkpoints", section "The format"
+ *     (qweight int32 [K*bits/32, N], codes along K, low bits first; qzeros int32
+ *     [G, N*bits/32], zeros along N, stored minus one; scales [G, N]; g_idx int32 [K]).
+ * Weights stay packed from HBM until they reach registers or shared memory; the dense W is
+ * never written to memory (mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin,
+ * Machete", opening section).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" must point to memory of the CUDA device that is current when the
+ *     call is made; pointers named "host" must be host memory.  No pointer is retained after a
+ *     call returns except inside a handle, which owns only memory it allocated itself.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Device
+ *     work is enqueued on it and is stream-ordered with the caller's other work.
+ *   - Every call returns a gptq_status_t.  Host-side argument checks happen before any device
+ *     work is enqueued; a failed check leaves every output untouched.  gptq_last_error_message
+ *     gives the text of the calling thread's last failure.  No call aborts, traps or asserts.
+ *   - Element types: x, y and scales share one dtype (fp16 or bf16) per handle.  Accumulation is
+ *     fp32; y is rounded to the dtype once, round-to-nearest-even.
+ */
+#ifndef GPTQ_GB300_H
+#define GPTQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gptq_handle_s* gptq_handle_t;
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_INVALID_ARG = 1,   /* null pointer, negative size, handle/device mismatch         */
+  GPTQ_ERR_UNSUPPORTED = 2,   /* bits not in {2,3,4,8} (GPTQ-001), dtype not fp16/bf16        */
+  GPTQ_ERR_SHAPE = 3,         /* tensor shapes break GPTQ-002 / GPTQ-003 / GPTQ-004 (length)  */
+  GPTQ_ERR_INVALID_GIDX = 4,  /* a g_idx value selects no scale/zero row (GPTQ-004)           */
+  GPTQ_ERR_ALIGNMENT = 5,     /* a pointer is not aligned as documented below                */
+  GPTQ_ERR_WORKSPACE = 6,     /* the call needs more workspace than gptq_reserve set up       */
+  GPTQ_ERR_CUDA = 7,          /* a CUDA runtime call or kernel launch failed                  */
+  GPTQ_ERR_DEVICE = 8,        /* the current device is not a compute capability 10.3 GPU     */
+  GPTQ_ERR_TIMEOUT = 9        /* a bounded device-side wait gave up (the context stays usable)*/
+} gptq_status_t;
+
+typedef enum { GPTQ_FP16 = 0, GPTQ_BF16 = 1 } gptq_dtype_t;
+
+/* Which kernel family gptq_gemm_path runs.  AUTO is what gptq_gemm does. */
+typedef enum { GPTQ_PATH_AUTO = 0, GPTQ_PATH_SMALL_M = 1, GPTQ_PATH_LARGE_M = 2 } gptq_path_t;
+
+/*
+ * Shape rules of "Reject the file when" applied to declared tensor shapes, before any data is
+ * touched.  Host only; safe without a GPU.
+ *   bits                 GPTQ-001: must be 2, 3, 4 or 8                     (else UNSUPPORTED)
+ *   qweight_rows/cols    GPTQ-002: qweight is [in_features/32*bits, out_features] and
+ *                        in_features % 32 == 0; in_features = qweight_rows*32/bits  (else SHAPE)
+ *   qzeros_rows/cols     GPTQ-003: qzeros_cols == out_features/32*bits; out_features must also be
+ *                        a multiple of 32 so that the floor in that rule is exact   (else SHAPE)
+ *                        qzeros_rows must equal G = ceil(in_features/group_size), or 1 when
+ *                        group_size == -1 ("one group covering in_features")       (else SHAPE)
+ *   scales_rows/cols     must be [G, out_features]                                  (else SHAPE)
+ *   g_idx_len            GPTQ-004: must equal in_features, or be 0 for "no g_idx" (else SHAPE)
+ *   group_size           -1 or >= 1                                          (else INVALID_ARG)
+ * On GPTQ_OK, *in_features and *out_features (if non-NULL) receive K and N.
+ */
+gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_cols,
+                                int64_t qzeros_rows, int64_t qzeros_cols,
+                                int64_t scales_rows, int64_t scales_cols, int64_t g_idx_len,
+                                int group_size, int* in_features, int* out_features);
+
+/*
+ * Build a runtime handle from one checkpoint layer (the "to_runtime" step of ch. 39, section
+ * "The format": input columns are sorted by g_idx once at load time so groups become
+ * contiguous, and activations are permuted to match at run time).
+ *
+ *   qweight  device, int32 [K*bits/32, N] row-major, codes along K, low bits first; for bits 3
+ *            the 10 / split / 10 word layout (32 codes in 3 consecutive words).  4-byte aligned.
+ *   qzeros   device, int32 [G, N*bits/32] row-major, zeros along N, each stored minus one
+ *            (GPTQ-006: the zero used is stored + 1, with no wrap).  4-byte aligned.
+ *   scales   device, dtype [G, N] row-major.  2-byte aligned.
+ *   g_idx    device, int32 [K], or NULL for the sequential k / group_size.  4-byte aligned.
+ *            Any values in [0, G) are accepted; each group's run in sorted order is padded to a
+ *            multiple of 32 rows internally, so uneven groups cost bandwidth but stay exact.
+ *   K, N     in_features and out_features: K % 32 == 0, N % 32 == 0, 32 <= K, N <= 1<<20.
+ *   bits     2, 3, 4 or 8.   group_size: -1 (one group) or >= 1; G = ceil(K/group_size).
+ *   dtype    dtype of scales, and of x and y in every later gptq_gemm on this handle.
+ *   stream   the copy/repack kernels run on it; the call synchronizes it once, at the end, to
+ *            read back the g_idx check.  The checkpoint buffers may be freed or changed as soon
+ *            as the call returns; the handle holds its own copy in its runtime layout.
+ *   out      receives the handle (set to NULL on failure).
+ * The handle allocates its runtime layout (about K*N*bits/8 bytes plus 3*G*N) and a workspace
+ * for gptq_gemm calls with M <= 16; gptq_reserve enlarges the workspace.  The handle is
+ * immutable: after any change to the weights, build a new one.
+ * Errors: INVALID_ARG, UNSUPPORTED, SHAPE, ALIGNMENT, DEVICE, INVALID_GIDX, CUDA.
+ */
+gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                          const int32_t* g_idx, int K, int N, int bits, int group_size,
+                          gptq_dtype_t dtype, void* stream, gptq_handle_t* out);
+
+/*
+ * Make gptq_gemm calls with M <= max_M possible without any allocation inside gptq_gemm.
+ * Only a handle whose g_idx order is not the identity (act-order, or groups whose sizes are
+ * not multiples of 32) needs workspace above M = 16: max_M * K_sorted activation elements for
+ * the permuted copy of x that the large-M kernel reads.  Allocates (cudaMalloc) outside any
+ * stream capture; never shrinks.  Errors: INVALID_ARG, CUDA.
+ */
+gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
+
+/*
+ * y = x . W^T for the handle's layer, enqueued on `stream`.
+ *   x   device, dtype [M, K] row-major (row stride K elements), 16-byte aligned.
+ *   y   device, dtype [M, N] row-major (row stride N elements), 16-byte aligned; x and y must
+ *       not overlap.
+ *   M   >= 0.  M == 0 returns GPTQ_OK and launches nothing.
+ * Never allocates and never synchronizes.  One handle may be used by one stream at a time
+ * (calls on two streams must not overlap on the device: they share the handle's workspace).
+ * After gptq_reserve(h, M) has returned, a call with that M may be captured in a CUDA graph.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE (M above the reserved size on a path that needs
+ * workspace), CUDA.
+ */
+gptq_status_t gptq_gemm(gptq_handle_t h, const void* x, void* y, int M, void* stream);
+
+/* As gptq_gemm, with the kernel family forced (AUTO = gptq_gemm's choice).  Both families give
+ * results within the same tolerance; this exists so each can be checked at any M. */
+gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gptq_path_t path,
+                             void* stream);
+
+/* Number of kernels one gptq_gemm_path call at this M launches (0 for M == 0), or -1 on a bad
+ * argument.  Host only. */
+int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
+
+/* Free the handle and everything it owns.  Waits for the device to finish using it
+ * (cudaDeviceSynchronize on the handle's device).  NULL is accepted. */
+gptq_status_t gptq_destroy(gptq_handle_t h);
+
+/* Sizes of a handle's runtime layout. */
+typedef struct {
+  int K, N, bits, group_size, G;
+  int K_sorted;     /* rows of the sorted, padded K order: a multiple of 128, >= K            */
+  int N_padded;     /* N rounded up to a multiple of 256                                      */
+  int identity;     /* 1 when the sorted order is k itself (no permutation, no padding)       */
+  gptq_dtype_t dtype;
+  int reserved_M;   /* largest M gptq_gemm accepts on every path without further reserve      */
+  size_t weight_bytes;     /* runtime codes: K_sorted/128 * bits * N_padded * 16              */
+  size_t device_bytes;     /* everything the handle holds on the device                      */
+} gptq_info_t;
+
+gptq_status_t gptq_get_info(gptq_handle_t h, gptq_info_t* info);
+
+/*
+ * Copy the runtime layout to host memory (synchronous), for checking the repack bit by bit.
+ *   wr    host, info.weight_bytes bytes        perm  host, int32 [K_sorted]
+ *   cgid  host, int32 [K_sorted/32]            s_r   host, dtype bits [G, N_padded]
+ *   z_r   host, uint8 [G, N_padded] (stored zero = zero - 1)
+ * Any pointer may be NULL to skip that buffer.  Errors: INVALID_ARG, CUDA.
+ */
+gptq_status_t gptq_copy_runtime(gptq_handle_t h, void* wr, int32_t* perm, int32_t* cgid,
+                                void* s_r, uint8_t* z_r);
+
+/* Static text for a status. */
+const char* gptq_status_string(gptq_status_t s);
+
+/* Text of the calling thread's most recent failure ("" if none).  Valid until the next call. */
+const char* gptq_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_GB300_H */

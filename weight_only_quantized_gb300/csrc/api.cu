@@ -1,0 +1,265 @@
+// Host side of the C ABI: argument checks (the reject rules of tensref.org "GPTQ packed
+// checkpoint", section "Reject the file when"), handle lifecycle, and the per-call M dispatch.
+#include "internal.cuh"
+
+#include <cstring>
+#include <new>
+#include <string>
+
+namespace gptq {
+
+namespace {
+thread_local std::string g_last_error;
+constexpr int kMaxK = 1 << 17;        // in_features limit (index arithmetic and repack cost)
+constexpr int kMaxN = 1 << 18;        // out_features limit
+constexpr int kMaxGroups = 1 << 16;
+// Largest M routed to the small-M (mma.sync weight-streaming) kernel by gptq_gemm.  At M <= 16
+// the layer is HBM-bound on GB300 (ridge M* = P * 4.125 / (16 * BW) ~ 72 for 4-bit group 128)
+// and the swap-AB mma.sync kernel keeps every SM streaming weights.
+constexpr int kSmallMMax = 16;
+}  // namespace
+
+gptq_status_t fail(gptq_status_t s, const std::string& msg) {
+  g_last_error = std::string(gptq_status_string(s)) + ": " + msg;
+  return s;
+}
+
+gptq_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(GPTQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                            const int32_t* g_idx, cudaStream_t st);
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static void free_handle(Handle* h) {
+  if (!h) return;
+  cudaFree(h->wr);
+  cudaFree(h->perm);
+  cudaFree(h->cgid);
+  cudaFree(h->s_r);
+  cudaFree(h->z_r);
+  cudaFree(h->xp);
+  delete h;
+}
+
+static gptq_status_t check_device(int* dev_out, int* sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(GPTQ_ERR_DEVICE, "this library is built for sm_103a (compute capability 10.3); device " +
+                                     std::to_string(dev) + " is " + std::to_string(major) + "." + std::to_string(minor));
+  *dev_out = dev;
+  *sms_out = sms;
+  return GPTQ_OK;
+}
+
+static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, gptq_path_t path, void* stream) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  if (M < 0) return fail(GPTQ_ERR_INVALID_ARG, "M must be >= 0");
+  if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M)
+    return fail(GPTQ_ERR_INVALID_ARG, "unknown path");
+  if (M == 0) return GPTQ_OK;   // an empty batch is a normal input: nothing to launch
+  if (!x || !y) return fail(GPTQ_ERR_INVALID_ARG, "x and y must be device pointers");
+  if (!aligned(x, 16) || !aligned(y, 16)) return fail(GPTQ_ERR_ALIGNMENT, "x and y must be 16-byte aligned");
+  const size_t es = 2;
+  const char* xb = static_cast<const char*>(x);
+  const char* yb = static_cast<const char*>(y);
+  if (xb < yb + (size_t)M * h.N * es && yb < xb + (size_t)M * h.K * es)
+    return fail(GPTQ_ERR_INVALID_ARG, "x and y overlap");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h.device)
+    return fail(GPTQ_ERR_INVALID_ARG, "handle belongs to device " + std::to_string(h.device) +
+                                          " but device " + std::to_string(dev) + " is current");
+  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  if (path == GPTQ_PATH_LARGE_M && !large_m_available())
+    return fail(GPTQ_ERR_UNSUPPORTED, "the large-M kernel is not part of this build");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (path == GPTQ_PATH_LARGE_M) {
+    if (!h.identity && M > h.reserved_M)
+      return fail(GPTQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs gptq_reserve(h, M): the handle's g_idx "
+                                      "order is not the identity and only M <= " + std::to_string(h.reserved_M) + " is reserved");
+    e = launch_gemm_large(h, x, y, M, st);
+  } else {
+    e = launch_gemm_small(h, x, y, M, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "gptq_gemm launch");
+  return GPTQ_OK;
+}
+
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" {
+
+const char* gptq_status_string(gptq_status_t s) {
+  switch (s) {
+    case GPTQ_OK: return "GPTQ_OK";
+    case GPTQ_ERR_INVALID_ARG: return "GPTQ_ERR_INVALID_ARG";
+    case GPTQ_ERR_UNSUPPORTED: return "GPTQ_ERR_UNSUPPORTED";
+    case GPTQ_ERR_SHAPE: return "GPTQ_ERR_SHAPE";
+    case GPTQ_ERR_INVALID_GIDX: return "GPTQ_ERR_INVALID_GIDX";
+    case GPTQ_ERR_ALIGNMENT: return "GPTQ_ERR_ALIGNMENT";
+    case GPTQ_ERR_WORKSPACE: return "GPTQ_ERR_WORKSPACE";
+    case GPTQ_ERR_CUDA: return "GPTQ_ERR_CUDA";
+    case GPTQ_ERR_DEVICE: return "GPTQ_ERR_DEVICE";
+    case GPTQ_ERR_TIMEOUT: return "GPTQ_ERR_TIMEOUT";
+  }
+  return "GPTQ_ERR_UNKNOWN";
+}
+
+const char* gptq_last_error_message(void) { return g_last_error.c_str(); }
+
+gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_cols, int64_t qzeros_rows,
+                                int64_t qzeros_cols, int64_t scales_rows, int64_t scales_cols, int64_t g_idx_len,
+                                int group_size, int* in_features, int* out_features) {
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8)
+    return fail(GPTQ_ERR_UNSUPPORTED, "GPTQ-001: bits must be 2, 3, 4 or 8, got " + std::to_string(bits));
+  if (group_size != -1 && group_size < 1)
+    return fail(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or >= 1, got " + std::to_string(group_size));
+  if (qweight_rows <= 0 || qweight_cols <= 0 || (qweight_rows * 32) % bits != 0)
+    return fail(GPTQ_ERR_SHAPE, "GPTQ-002: qweight rows must be in_features // 32 * bits");
+  const int64_t K = qweight_rows * 32 / bits, N = qweight_cols;
+  if (K % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-002: in_features must be divisible by 32");
+  if (N % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a multiple of 32 (qzeros width N/32*bits)");
+  if (qzeros_cols != N / 32 * bits)
+    return fail(GPTQ_ERR_SHAPE, "GPTQ-003: qzeros.shape[1] must be out_features // 32 * bits = " + std::to_string(N / 32 * bits));
+  const int64_t G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
+  if (qzeros_rows != G)
+    return fail(GPTQ_ERR_SHAPE, "qzeros.shape[0] must be ceil(in_features / group_size) = " + std::to_string(G));
+  if (scales_rows != G || scales_cols != N)
+    return fail(GPTQ_ERR_SHAPE, "scales must be [ceil(in_features / group_size), out_features]");
+  if (g_idx_len != 0 && g_idx_len != K)
+    return fail(GPTQ_ERR_SHAPE, "GPTQ-004: g_idx length must equal in_features = " + std::to_string(K));
+  if (K > kMaxK || N > kMaxN || G > kMaxGroups)
+    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= 131072, N <= 262144, groups <= 65536)");
+  if (in_features) *in_features = (int)K;
+  if (out_features) *out_features = (int)N;
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
+                          int K, int N, int bits, int group_size, gptq_dtype_t dtype, void* stream,
+                          gptq_handle_t* out) {
+  if (!out) return fail(GPTQ_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!qweight || !qzeros || !scales) return fail(GPTQ_ERR_INVALID_ARG, "qweight, qzeros and scales are required");
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8)
+    return fail(GPTQ_ERR_UNSUPPORTED, "GPTQ-001: bits must be 2, 3, 4 or 8, got " + std::to_string(bits));
+  if (dtype != GPTQ_FP16 && dtype != GPTQ_BF16) return fail(GPTQ_ERR_UNSUPPORTED, "dtype must be GPTQ_FP16 or GPTQ_BF16");
+  if (group_size != -1 && group_size < 1)
+    return fail(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or >= 1, got " + std::to_string(group_size));
+  if (K < 32 || K % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-002: in_features must be a positive multiple of 32");
+  if (N < 32 || N % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a positive multiple of 32");
+  const int G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
+  if (K > kMaxK || N > kMaxN || G > kMaxGroups)
+    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= 131072, N <= 262144, groups <= 65536)");
+  if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, 2) || (g_idx && !aligned(g_idx, 4)))
+    return fail(GPTQ_ERR_ALIGNMENT, "qweight, qzeros, g_idx need 4-byte and scales 2-byte alignment");
+  int dev = 0, sms = 0;
+  gptq_status_t s = check_device(&dev, &sms);
+  if (s != GPTQ_OK) return s;
+  Handle* h = new (std::nothrow) Handle();
+  if (!h) return fail(GPTQ_ERR_INVALID_ARG, "out of host memory");
+  h->device = dev;
+  h->sm_count = sms;
+  h->K = K; h->N = N; h->bits = bits; h->group_size = group_size; h->G = G;
+  h->Np = (N + 255) / 256 * 256;
+  h->dtype = dtype;
+  s = build_runtime(*h, qweight, qzeros, scales, g_idx, static_cast<cudaStream_t>(stream));
+  if (s != GPTQ_OK) { free_handle(h); return s; }
+  h->reserved_M = 0;
+  s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 16);
+  if (s != GPTQ_OK) { free_handle(h); return s; }
+  *out = reinterpret_cast<gptq_handle_t>(h);
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  if (max_M < 0) return fail(GPTQ_ERR_INVALID_ARG, "max_M must be >= 0");
+  Handle& h = *reinterpret_cast<Handle*>(hh);
+  if (max_M <= h.reserved_M) return GPTQ_OK;
+  if (!h.identity) {
+    const size_t bytes = (size_t)max_M * h.Kr * 2;
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(gptq_reserve workspace)");
+    cudaFree(h.xp);
+    h.xp = p;
+    h.xp_bytes = bytes;
+  }
+  h.reserved_M = max_M;
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_gemm(gptq_handle_t h, const void* x, void* y, int M, void* stream) {
+  return gemm_impl(h, x, y, M, GPTQ_PATH_AUTO, stream);
+}
+
+gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gptq_path_t path, void* stream) {
+  return gemm_impl(h, x, y, M, path, stream);
+}
+
+int gptq_gemm_launches(gptq_handle_t hh, int M, gptq_path_t path) {
+  if (!hh || M < 0) return -1;
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  if (M == 0) return 0;
+  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  return path == GPTQ_PATH_LARGE_M ? large_m_launches(h, M) : small_m_launches(h, M);
+}
+
+gptq_status_t gptq_destroy(gptq_handle_t hh) {
+  if (!hh) return GPTQ_OK;
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  const int dev = h->device;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != dev) cudaSetDevice(dev);
+  cudaError_t e = cudaDeviceSynchronize();
+  free_handle(h);
+  if (cur >= 0 && cur != dev) cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "gptq_destroy: cudaDeviceSynchronize");
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
+  if (!hh || !info) return fail(GPTQ_ERR_INVALID_ARG, "handle and info are required");
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  info->K = h.K; info->N = h.N; info->bits = h.bits; info->group_size = h.group_size; info->G = h.G;
+  info->K_sorted = h.Kr; info->N_padded = h.Np; info->identity = h.identity; info->dtype = h.dtype;
+  info->reserved_M = h.reserved_M;
+  info->weight_bytes = h.wr_bytes();
+  info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
+                       (size_t)h.G * h.Np * 3 + h.xp_bytes;
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_copy_runtime(gptq_handle_t hh, void* wr, int32_t* perm, int32_t* cgid, void* s_r, uint8_t* z_r) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  cudaError_t e = cudaSuccess;
+  if (wr && (e = cudaMemcpy(wr, h.wr, h.wr_bytes(), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "copy wr");
+  if (perm && (e = cudaMemcpy(perm, h.perm, sizeof(int32_t) * h.Kr, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "copy perm");
+  if (cgid && (e = cudaMemcpy(cgid, h.cgid, sizeof(int32_t) * (h.Kr / 32), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "copy cgid");
+  if (s_r && (e = cudaMemcpy(s_r, h.s_r, 2 * (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "copy s_r");
+  if (z_r && (e = cudaMemcpy(z_r, h.z_r, (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "copy z_r");
+  return GPTQ_OK;
+}
+
+}  // extern "C"

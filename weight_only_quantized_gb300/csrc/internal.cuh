@@ -1,0 +1,76 @@
+// Internal declarations shared by the translation units of the GPTQ library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+#include <string>
+
+#include "../../include/gptq.h"
+
+namespace gptq {
+
+// Runtime handle: the checkpoint re-laid for the kernels (see repack.cu for the layout).
+struct Handle {
+  int device = 0;
+  int K = 0, N = 0, bits = 0, group_size = 0, G = 0;
+  int Kr = 0;          // rows of the sorted, padded K order (multiple of 128)
+  int Np = 0;          // N padded to a multiple of 256
+  int identity = 0;    // sorted order == k and Kr == K
+  gptq_dtype_t dtype = GPTQ_FP16;
+  int sm_count = 0;
+  // runtime layout
+  uint8_t* wr = nullptr;     // codes: [Kr/128][bits vectors][Np][16 B]
+  int32_t* perm = nullptr;   // [Kr], -1 for pad rows
+  int32_t* cgid = nullptr;   // [Kr/32] group of each 32-row chunk
+  uint16_t* s_r = nullptr;   // [G][Np] scale bits
+  uint8_t* z_r = nullptr;    // [G][Np] stored zero (zero - 1)
+  // workspace
+  int reserved_M = 0;
+  void* xp = nullptr;        // [reserved_M][Kr] activations in sorted order (large-M path)
+  size_t xp_bytes = 0;
+  size_t wr_bytes() const { return (size_t)Kr / 128 * bits * Np * 16; }
+};
+
+// Status with message, recorded per thread.
+gptq_status_t fail(gptq_status_t s, const std::string& msg);
+gptq_status_t cuda_fail(cudaError_t e, const char* what);
+
+// ---- kernels launched from the host code (defined in the .cu files) ----
+cudaError_t launch_repack(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                          const int32_t* g_idx, cudaStream_t st, int* err_host_flags);
+
+// Small-M path: mma.sync (swap-AB) kernel with split-K reduced inside a thread-block cluster.
+int small_m_launches(const Handle& h, int M);
+cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
+
+// Large-M path: tcgen05 / TMEM / TMA kernel (plus an x-permute pre-pass when not identity).
+bool large_m_available();
+int large_m_launches(const Handle& h, int M);
+cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
+
+// ---- device helpers ----
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+}  // namespace gptq

@@ -1,0 +1,259 @@
+// Repack: checkpoint layout -> the kernel-private runtime layout (runs once per layer, at load).
+//
+// The checkpoint is the AutoGPTQ "cuda" pack (tensref.org "GPTQ packed checkpoint", sections
+// GptqLayer and Reader).  The runtime layout follows the loader of inference.shantanugoel.com
+// ch. 39 "Quantized checkpoints", section "The format": input columns are sorted by g_idx once,
+// so that groups become contiguous, and x is permuted to match at run time.
+//
+// Runtime layout (every kernel reads exactly this):
+//  * Sorted, padded K.  Each group's run of input features (ascending k inside the group) is
+//    padded to a multiple of 32 rows; the total is padded to Kr, a multiple of 128.  perm[j]
+//    is the input feature of sorted row j, or -1 for a pad row (its activation is 0).
+//    cgid[c] is the group of the 32-row chunk c; chunks after the last real row take the last
+//    real chunk's group.
+//  * N padded to Np (multiple of 256); pad columns hold code 0, stored zero 0, scale 0.
+//  * Codes: in blocks of 128 sorted rows.  Inside block B, row r = j % 128 has chunk c = r/32,
+//    lane t = (r%32)/8 and e = r%8; it is element e%2 ("half" h) of pair p = 4c + e/2 of lane t.
+//    A plane of bp bits per code holds F = 16/bp fields in each 16-bit half of a word; pair p
+//    lives in lane word jw = p/F, field f = p%F, at bit 16h + bp*f.  Lane t owns words
+//    q = t*bp .. t*bp + bp-1; word q sits in 16-byte vector q/4, slot q%4.  Vectors of one
+//    (block, column) are stored [B][vector][column][16 bytes], plane after plane.
+//    bits 2/4/8 use one plane (bp = bits); bits 3 uses a 2-bit plane (code & 3) followed by a
+//    1-bit plane (code >> 2), in the spirit of GPTQModel's planar packing (fields never
+//    straddle words), a layout chosen for the decoder, not a checkpoint format.
+//    Why: the two 16-bit halves of a word give the two bf16/fp16 lanes of one register after a
+//    single mask-and-or with a magic exponent, and lane t's pairs are exactly the k indices an
+//    mma.sync m16n8k16 A-fragment row needs after a fixed relabelling of k, while a whole
+//    128-row block of one column is 16*bits contiguous-by-vector bytes for the large-M loader.
+//  * s_r[g][n]: scale bits; z_r[g][n]: stored zero (zero - 1) as one byte.
+#include "internal.cuh"
+
+#include <vector>
+
+namespace gptq {
+namespace {
+
+// Code k of a packed column: the column's words read as one little-endian bit string, code k at
+// bits [bits*k, bits*k + bits).  For bits 2/4/8 that is "word k / (32/bits), shifted by
+// bits*(k % (32/bits))" (the Reader); for bits 3 it is the 10 / split / 10 word layout, where
+// codes 10 and 21 of each 32 straddle a word boundary.
+__device__ __forceinline__ uint32_t column_code(const int32_t* __restrict__ words, long stride, long k, int bits) {
+  long bit = (long)bits * k;
+  long row = bit >> 5;
+  int sh = (int)(bit & 31);
+  uint32_t v = (uint32_t)__ldg(&words[row * stride]) >> sh;
+  if (sh + bits > 32) v |= (uint32_t)__ldg(&words[(row + 1) * stride]) << (32 - sh);
+  return v & ((1u << bits) - 1u);
+}
+
+__device__ __forceinline__ int group_of(const int32_t* __restrict__ g_idx, int k, int group_size) {
+  if (g_idx) return __ldg(&g_idx[k]);
+  return group_size == -1 ? 0 : k / group_size;
+}
+
+// meta[] slots written by k_histogram
+enum { M_BAD_GIDX = 0, M_NONDECR = 1, M_KS = 2, M_KR = 3, M_LAST_G = 4, M_ALL32 = 5, M_BAD_K = 6, M_N = 8 };
+
+// One block: histogram of g_idx, range check, padded exclusive scan of the group runs.
+__global__ void k_histogram(const int32_t* __restrict__ g_idx, int K, int G, int group_size,
+                            int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ meta) {
+  __shared__ int s_bad, s_nondecr, s_last, s_all32, s_bad_k;
+  __shared__ long s_carry;
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) { s_bad = 0; s_nondecr = 1; s_last = -1; s_all32 = 1; s_bad_k = -1; s_carry = 0; }
+  for (int g = tid; g < G; g += nt) cnt[g] = 0;
+  __syncthreads();
+  for (int k = tid; k < K; k += nt) {
+    int g = group_of(g_idx, k, group_size);
+    if (g < 0 || g >= G) {
+      atomicExch(&s_bad, 1);
+      atomicMax(&s_bad_k, k);
+      continue;
+    }
+    atomicAdd(&cnt[g], 1);
+    atomicMax(&s_last, g);
+    if (k > 0 && group_of(g_idx, k - 1, group_size) > g) atomicExch(&s_nondecr, 0);
+  }
+  __syncthreads();
+  // exclusive scan of roundup(cnt, 32), 1024 groups at a time
+  for (int base = 0; base < G; base += nt) {
+    int g = base + tid;
+    int c = g < G ? cnt[g] : 0;
+    if (c % 32) atomicExch(&s_all32, 0);
+    int v = (c + 31) / 32 * 32;
+    // inclusive scan inside the warp
+    int lane = tid & 31, w = tid >> 5;
+    int x = v;
+    for (int d = 1; d < 32; d <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int nw = nt / 32;
+      int y = lane < nw ? s_warp[lane] : 0;
+      for (int d = 1; d < 32; d <<= 1) {
+        int z = __shfl_up_sync(0xffffffffu, y, d);
+        if (lane >= d) y += z;
+      }
+      if (lane < nw) s_warp[lane] = y;       // inclusive scan of warp totals
+    }
+    __syncthreads();
+    long before = s_carry + (w > 0 ? s_warp[w - 1] : 0) + (x - v);
+    if (g < G) off[g] = (int32_t)before;
+    __syncthreads();
+    if (tid == nt - 1) s_carry += s_warp[nt / 32 - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    long Ks = s_carry;
+    meta[M_BAD_GIDX] = s_bad;
+    meta[M_NONDECR] = s_nondecr;
+    meta[M_KS] = (int32_t)Ks;
+    meta[M_KR] = (int32_t)((Ks + 127) / 128 * 128);
+    meta[M_LAST_G] = s_last;
+    meta[M_ALL32] = s_all32;
+    meta[M_BAD_K] = s_bad_k;
+  }
+}
+
+// One warp: stable scatter of every k to its sorted row.  32 consecutive k at a time; lanes that
+// share a group take consecutive slots in ascending k (rank = earlier peers in the warp).
+__global__ void k_scatter_perm(const int32_t* __restrict__ g_idx, int K, int group_size,
+                               const int32_t* __restrict__ off, int32_t* __restrict__ cursor,
+                               int32_t* __restrict__ perm) {
+  const int lane = threadIdx.x;
+  for (int base = 0; base < K; base += 32) {
+    const int k = base + lane;                  // K % 32 == 0: every lane has a k
+    const int g = group_of(g_idx, k, group_size);
+    const unsigned peers = __match_any_sync(0xffffffffu, g);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    const int b = *(volatile int32_t*)&cursor[g];
+    perm[off[g] + b + rank] = k;
+    __syncwarp();
+    if (lane == leader) *(volatile int32_t*)&cursor[g] = b + __popc(peers);
+    __syncwarp();
+  }
+}
+
+// One thread per group: pad rows of its run, chunk group ids, and the trailing pad chunks.
+__global__ void k_pads(int G, int Ks, int Kr, int last_g, const int32_t* __restrict__ cnt,
+                       const int32_t* __restrict__ off, int32_t* __restrict__ perm, int32_t* __restrict__ cgid) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  const int c = cnt[g], j0 = off[g], run = (c + 31) / 32 * 32;
+  for (int j = j0 + c; j < j0 + run; ++j) perm[j] = -1;
+  for (int ch = j0 / 32; ch < (j0 + run) / 32; ++ch) cgid[ch] = g;
+  if (g == last_g) {
+    for (int j = Ks; j < Kr; ++j) perm[j] = -1;
+    for (int ch = Ks / 32; ch < Kr / 32; ++ch) cgid[ch] = g;
+  }
+}
+
+// One thread per (block B, vector V, column n): assembles that 16-byte vector.
+__global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t* __restrict__ perm,
+                             int N, int Np, int bits, int nBV, uint8_t* __restrict__ wr) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= Np) return;
+  for (int by = blockIdx.y; by < nBV; by += gridDim.y) {
+  const int B = by / bits, V = by % bits;
+  int bp, v, plane;
+  if (bits == 3) { plane = V < 2 ? 0 : 1; bp = plane == 0 ? 2 : 1; v = plane == 0 ? V : 0; }
+  else { plane = 0; bp = bits; v = V; }
+  const int F = 16 / bp;
+  uint32_t out[4];
+#pragma unroll 1
+  for (int w = 0; w < 4; ++w) {
+    const int q = 4 * v + w, t = q / bp, jw = q % bp;
+    uint32_t word = 0;
+    for (int h = 0; h < 2; ++h)
+      for (int f = 0; f < F; ++f) {
+        const int p = jw * F + f, c = p / 4, e = 2 * (p % 4) + h;
+        const int jj = 128 * B + 32 * c + 8 * t + e;
+        const int k = __ldg(&perm[jj]);
+        uint32_t code = (k >= 0 && n < N) ? column_code(qweight + n, N, k, bits) : 0u;
+        uint32_t val = bits == 3 ? (plane == 0 ? (code & 3u) : (code >> 2)) : code;
+        word |= val << (16 * h + bp * f);
+      }
+    out[w] = word;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(wr + (((size_t)B * bits + V) * Np + n) * 16);
+  *dst = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// One thread per (group, column): scale bits and stored zero.
+__global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales,
+                          int N, int Np, int bits, int G, uint16_t* __restrict__ s_r, uint8_t* __restrict__ z_r) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= Np) return;
+  const long wpr = (long)N * bits / 32;
+  for (int g = blockIdx.y; g < G; g += gridDim.y) {
+  uint16_t s = 0;
+  uint8_t z = 0;
+  if (n < N) {
+    s = __ldg(&scales[(long)g * N + n]);
+    z = (uint8_t)column_code(qzeros + (long)g * wpr, 1, n, bits);
+  }
+  s_r[(long)g * Np + n] = s;
+  z_r[(long)g * Np + n] = z;
+  }
+}
+
+}  // namespace
+
+gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                            const int32_t* g_idx, cudaStream_t st) {
+  const int K = h.K, N = h.N, G = h.G;
+  int32_t* tmp = nullptr;   // cnt[G] | off[G] | cursor[G] | meta[M_N]
+  cudaError_t e = cudaMalloc(&tmp, sizeof(int32_t) * ((size_t)3 * G + M_N));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(repack scratch)");
+  int32_t* cnt = tmp;
+  int32_t* off = tmp + G;
+  int32_t* cursor = tmp + 2 * (size_t)G;
+  int32_t* meta = tmp + 3 * (size_t)G;
+  int32_t meta_h[M_N] = {};
+  auto cleanup = [&]() { cudaFree(tmp); };
+
+  k_histogram<<<1, 1024, 0, st>>>(g_idx, K, G, h.group_size, cnt, off, meta);
+  if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "histogram launch"); }
+  if ((e = cudaMemcpyAsync(meta_h, meta, sizeof(meta_h), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "repack: reading the g_idx histogram");
+  }
+  if (meta_h[M_BAD_GIDX]) {
+    cleanup();
+    return fail(GPTQ_ERR_INVALID_GIDX, "GPTQ-004: g_idx[" + std::to_string(meta_h[M_BAD_K]) +
+                                           "] selects no scale/zero row (valid groups are 0.." + std::to_string(G - 1) + ")");
+  }
+  h.Kr = meta_h[M_KR];
+  h.identity = meta_h[M_NONDECR] && meta_h[M_ALL32] && h.Kr == K;
+  const int Ks = meta_h[M_KS], last_g = meta_h[M_LAST_G];
+
+  size_t wr_b = h.wr_bytes();
+  if ((e = cudaMalloc(&h.wr, wr_b)) != cudaSuccess || (e = cudaMalloc(&h.perm, sizeof(int32_t) * h.Kr)) != cudaSuccess ||
+      (e = cudaMalloc(&h.cgid, sizeof(int32_t) * (h.Kr / 32))) != cudaSuccess ||
+      (e = cudaMalloc(&h.s_r, sizeof(uint16_t) * (size_t)G * h.Np)) != cudaSuccess ||
+      (e = cudaMalloc(&h.z_r, (size_t)G * h.Np)) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "cudaMalloc(runtime layout)");
+  }
+  if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * G, st)) != cudaSuccess) { cleanup(); return cuda_fail(e, "memset"); }
+  k_scatter_perm<<<1, 32, 0, st>>>(g_idx, K, h.group_size, off, cursor, h.perm);
+  k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, h.Kr, last_g, cnt, off, h.perm, h.cgid);
+  const int nBV = (h.Kr / 128) * h.bits;
+  dim3 gc(h.Np / 256, nBV < 65535 ? nBV : 65535);
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, h.wr);
+  dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, h.s_r, h.z_r);
+  if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack"); }
+  cleanup();
+  return GPTQ_OK;
+}
+
+}  // namespace gptq

@@ -1,0 +1,204 @@
+"""Python binding of the C ABI in include/gptq.h (argument marshalling only).
+
+Every function here has the C entry point's name and does nothing but turn torch
+tensors into pointers and sizes, call the library, and raise on a non-OK status.
+All work runs in the CUDA library; there is no Python or CPU fallback: if the
+library cannot be built or loaded, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GPTQ_OK = 0
+STATUS = {0: "GPTQ_OK", 1: "GPTQ_ERR_INVALID_ARG", 2: "GPTQ_ERR_UNSUPPORTED", 3: "GPTQ_ERR_SHAPE",
+          4: "GPTQ_ERR_INVALID_GIDX", 5: "GPTQ_ERR_ALIGNMENT", 6: "GPTQ_ERR_WORKSPACE", 7: "GPTQ_ERR_CUDA",
+          8: "GPTQ_ERR_DEVICE", 9: "GPTQ_ERR_TIMEOUT"}
+PATH_AUTO, PATH_SMALL_M, PATH_LARGE_M = 0, 1, 2
+DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+
+_lock = threading.Lock()
+_lib = None
+
+# Every symbol include/gptq.h declares, with its ctypes signature.
+_P, _I, _L = C.c_void_p, C.c_int, C.c_int64
+
+
+class GptqInfo(C.Structure):
+    _fields_ = [("K", C.c_int), ("N", C.c_int), ("bits", C.c_int), ("group_size", C.c_int), ("G", C.c_int),
+                ("K_sorted", C.c_int), ("N_padded", C.c_int), ("identity", C.c_int), ("dtype", C.c_int),
+                ("reserved_M", C.c_int), ("weight_bytes", C.c_size_t), ("device_bytes", C.c_size_t)]
+
+
+SIGNATURES = {
+    "gptq_check_shapes": (_I, [_I, _L, _L, _L, _L, _L, _L, _L, _I, _P, _P]),
+    "gptq_repack": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "gptq_reserve": (_I, [_P, _I]),
+    "gptq_gemm": (_I, [_P, _P, _P, _I, _P]),
+    "gptq_gemm_path": (_I, [_P, _P, _P, _I, _I, _P]),
+    "gptq_gemm_launches": (_I, [_P, _I, _I]),
+    "gptq_destroy": (_I, [_P]),
+    "gptq_get_info": (_I, [_P, C.POINTER(GptqInfo)]),
+    "gptq_copy_runtime": (_I, [_P, _P, _P, _P, _P, _P]),
+    "gptq_status_string": (C.c_char_p, [_I]),
+    "gptq_last_error_message": (C.c_char_p, []),
+}
+
+
+def lib():
+    """The loaded CUDA library (built in-tree on first use if missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = C.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype, f.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+class GptqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def _check(status: int):
+    if status != GPTQ_OK:
+        msg = lib().gptq_last_error_message().decode()
+        raise GptqError(status, msg or STATUS.get(status, str(status)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def gptq_status_string(status: int) -> str:
+    return lib().gptq_status_string(status).decode()
+
+
+def gptq_last_error_message() -> str:
+    return lib().gptq_last_error_message().decode()
+
+
+def gptq_check_shapes(bits: int, qweight_shape, qzeros_shape, scales_shape, g_idx_len: int,
+                      group_size: int) -> tuple[int, int]:
+    K, N = C.c_int(), C.c_int()
+    _check(lib().gptq_check_shapes(bits, qweight_shape[0], qweight_shape[1], qzeros_shape[0], qzeros_shape[1],
+                                   scales_shape[0], scales_shape[1], g_idx_len, group_size, C.byref(K), C.byref(N)))
+    return K.value, N.value
+
+
+class Handle:
+    """Owns one runtime handle; gptq_destroy runs when it is closed or collected."""
+
+    def __init__(self, raw: int):
+        self.raw = raw
+
+    def close(self):
+        if self.raw:
+            _check(lib().gptq_destroy(C.c_void_p(self.raw)))
+            self.raw = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def ptr(self):
+        if not self.raw:
+            raise GptqError(1, "handle is closed")
+        return C.c_void_p(self.raw)
+
+
+def gptq_repack(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor, g_idx: Optional[torch.Tensor],
+                bits: int, group_size: int, stream=None) -> Handle:
+    """Checkpoint tensors (on the current CUDA device) -> runtime handle."""
+    K, N = gptq_check_shapes(bits, tuple(qweight.shape), tuple(qzeros.shape), tuple(scales.shape),
+                             0 if g_idx is None else g_idx.numel(), group_size)
+    for name, t, dt in (("qweight", qweight, torch.int32), ("qzeros", qzeros, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise GptqError(1, f"{name} must be a contiguous int32 CUDA tensor")
+    if scales.dtype not in DTYPE or not scales.is_contiguous() or not scales.is_cuda:
+        raise GptqError(2, "scales must be a contiguous fp16 or bf16 CUDA tensor")
+    if g_idx is not None and (g_idx.dtype != torch.int32 or not g_idx.is_contiguous() or not g_idx.is_cuda):
+        raise GptqError(1, "g_idx must be a contiguous int32 CUDA tensor")
+    out = C.c_void_p()
+    _check(lib().gptq_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
+                             DTYPE[scales.dtype], _stream(stream), C.byref(out)))
+    return Handle(out.value)
+
+
+def gptq_reserve(h: Handle, max_M: int):
+    _check(lib().gptq_reserve(h.ptr, max_M))
+
+
+def gptq_gemm(h: Handle, x: torch.Tensor, y: torch.Tensor, M: Optional[int] = None, stream=None):
+    """y[:M] = x[:M] . W^T on the stream (default: torch's current stream)."""
+    M = x.shape[0] if M is None else M
+    _check(lib().gptq_gemm(h.ptr, _ptr(x), _ptr(y), M, _stream(stream)))
+
+
+def gptq_gemm_path(h: Handle, x: torch.Tensor, y: torch.Tensor, path: int, M: Optional[int] = None, stream=None):
+    M = x.shape[0] if M is None else M
+    _check(lib().gptq_gemm_path(h.ptr, _ptr(x), _ptr(y), M, path, _stream(stream)))
+
+
+def gptq_gemm_launches(h: Handle, M: int, path: int = PATH_AUTO) -> int:
+    return lib().gptq_gemm_launches(h.ptr, M, path)
+
+
+def gptq_destroy(h: Handle):
+    h.close()
+
+
+def gptq_get_info(h: Handle) -> GptqInfo:
+    info = GptqInfo()
+    _check(lib().gptq_get_info(h.ptr, C.byref(info)))
+    return info
+
+
+def gptq_copy_runtime(h: Handle) -> dict:
+    """The handle's runtime layout, copied to host numpy arrays."""
+    import numpy as np
+    info = gptq_get_info(h)
+    out = dict(Kr=info.K_sorted, Np=info.N_padded, G=info.G,
+               wr=np.empty(info.weight_bytes, np.uint8), perm=np.empty(info.K_sorted, np.int32),
+               cgid=np.empty(info.K_sorted // 32, np.int32), s_r=np.empty((info.G, info.N_padded), np.uint16),
+               z_r=np.empty((info.G, info.N_padded), np.uint8))
+    p = lambda a: a.ctypes.data_as(C.c_void_p)
+    _check(lib().gptq_copy_runtime(h.ptr, p(out["wr"]), p(out["perm"]), p(out["cgid"]), p(out["s_r"]), p(out["z_r"])))
+    return out
+
+
+class GptqLinear:
+    """A GPTQ linear layer on the current CUDA device: repack once, then y = layer(x)."""
+
+    def __init__(self, qweight, qzeros, scales, g_idx, bits: int, group_size: int, stream=None):
+        self.handle = gptq_repack(qweight, qzeros, scales, g_idx, bits, group_size, stream)
+        info = gptq_get_info(self.handle)
+        self.K, self.N, self.dtype = info.K, info.N, scales.dtype
+
+    def __call__(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if x.dtype != self.dtype or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise GptqError(1, f"x must be a contiguous [M, {self.K}] {self.dtype} tensor")
+        y = out if out is not None else torch.empty((x.shape[0], self.N), dtype=self.dtype, device=x.device)
+        gptq_gemm(self.handle, x, y, x.shape[0], stream)
+        return y
