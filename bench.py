@@ -1,0 +1,425 @@
+"""Benchmark of the GB300 GPTQ linear layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+One step is one gptq_gemm call (the whole per-call hot path: activation gather, packed-weight
+stream, dequant, MMA, split-K reduction, y store) on the Llama-3-8B-shaped decode layer
+(K=4096, N=14336, 4-bit, group 128, symmetric zero 8, bf16) at M=1.  Successive steps use
+successive weight sets of a 16-layer resident stack, so the working set (489 MB) is larger
+than L2 and no step reads weights another step left in L2.  Inputs are synthetic and seeded.
+
+value  = algorithmic bytes moved per call (packed weights + scales + packed zeros + x + y)
+         divided by the time per call, summed over ranks (one replica per GPU).
+e2e    = the same metric through the public API with host buffers: pinned x copied to the
+         device, gptq_gemm, y copied back, every step.
+Also reported (rank 0): the 70B gate_proj layer at M=1 and the prefill layer at M=4096, and the
+oracle timed on the host cores (cpu_baseline).
+
+--impl reference times the CPU oracle (the only reference this build has: the pages publish
+no runnable code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama3-8b-decode-4096x14336-b4g128-sym"
+METRIC = "GPTQ W4A16 GEMM µs/call, HBM GB/s (M=1), TFLOP/s (M=4096), % roofline"
+LAYERS = 16
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def b_alg(spec, M: int) -> int:
+    """Algorithmic bytes of one call: what the method has to move."""
+    K, N, b, G = spec.K, spec.N, spec.bits, spec.G
+    return K * N * b // 8 + 2 * G * N + G * N * b // 8 + (4 * K if spec.desc_act else 0) + 2 * M * K + 2 * M * N
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "weight_only_quantized_gb300", "csrc", kernel_file), "rb").read()
+        if rec.get(kernel_file, {}).get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return rec[kernel_file]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 8:
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [r for r in rows if r[3] not in ("0", "[N/A]")] or rows
+        mhz = [float(r[1]) for r in busy if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(busy)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v: float) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample_rate(spec, M: int, seconds: float, cols_per_call: int):
+    """Oracle GB/s on column samples of the workload: bytes scaled by the sampled fraction."""
+    import numpy as np
+
+    import oracle
+    from weight_only_quantized_gb300 import synth
+    ck = synth.make_checkpoint(spec, seed=0)
+    x = synth.make_x(M, spec.K, spec.dtype, seed=1)
+    cols_per_call = min(cols_per_call, spec.N)
+    rng = np.random.default_rng(0)
+    calls, t_total = 0, 0.0
+    while t_total < seconds or calls == 0:
+        cols = np.sort(rng.choice(spec.N, cols_per_call, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.linear(ck.qweight, ck.qzeros, ck.scales, ck.g_idx, spec.bits, spec.group_size, spec.dtype, x,
+                      None, cols)
+        t_total += time.perf_counter() - t0
+        calls += 1
+    frac = cols_per_call / spec.N
+    gbs = b_alg(spec, M) * frac * calls / t_total / 1e9
+    return gbs, calls, t_total, oracle.num_threads(), f"{calls} oracle calls on {cols_per_call} of {spec.N} output columns (all K, M={M}), {t_total:.1f} s"
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    from weight_only_quantized_gb300 import synth
+    spec, _ = synth.workload(WORKLOAD)
+    M = 1
+    # each step: one oracle call on a fixed-size column sample
+    cols = 512
+    import numpy as np
+    import oracle
+    ck = synth.make_checkpoint(spec, seed=0)
+    x = synth.make_x(M, spec.K, spec.dtype, seed=1)
+    rng = np.random.default_rng(0)
+    for _ in range(max(0, args.warmup - 1)):
+        c = np.sort(rng.choice(spec.N, cols, replace=False)).astype(np.int32)
+        oracle.linear(ck.qweight, ck.qzeros, ck.scales, None, spec.bits, spec.group_size, spec.dtype, x, None, c)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        c = np.sort(rng.choice(spec.N, cols, replace=False)).astype(np.int32)
+        oracle.linear(ck.qweight, ck.qzeros, ck.scales, None, spec.bits, spec.group_size, spec.dtype, x, None, c)
+    dt = time.perf_counter() - t0
+    frac = cols / spec.N
+    value = b_alg(spec, M) * frac * args.steps / dt / 1e9
+    sample = f"each step: oracle on {cols} of {spec.N} output columns, all K, M={M}; bytes scaled by {frac:.4f}"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "K": spec.K, "N": spec.N, "bits": spec.bits,
+                       "group_size": spec.group_size, "parallelism": "rank 0 only (host cores)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- native arm
+def make_layers(spec, count, seed0=0):
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    hs, cks = [], []
+    for i in range(count):
+        ck = synth.make_checkpoint(spec, seed=seed0 + i)
+        h = gptq.gptq_repack(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(),
+                             None if ck.g_idx is None else ck.g_idx.cuda(), spec.bits, spec.group_size)
+        hs.append(h)
+        cks.append(ck)
+    torch.cuda.synchronize()
+    return hs, cks
+
+
+def time_calls(hs, xs, ys, M, steps, warmup, graph=True):
+    """Average per-call device time (s) of `steps` calls rotating over the handles.
+
+    graph=True: the `steps` calls are captured once into a CUDA graph (how a decode step is
+    deployed) and the timed region is one replay, bracketed by CUDA events on the replay stream.
+    graph=False: eager launches from the host, events around the loop."""
+    import torch
+    from weight_only_quantized_gb300 import gptq
+    n = len(hs)
+    st = torch.cuda.current_stream()
+    for i in range(warmup):
+        gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M, st)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(steps):
+                gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M)
+        torch.cuda.synchronize()
+        g.replay()                      # untimed replay: graph upload and first-touch effects
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        t0.record(st)
+        g.replay()
+        t1.record(st)
+        torch.cuda.synchronize()
+        del g
+    else:
+        t0.record(st)
+        for i in range(steps):
+            gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M, st)
+        t1.record(st)
+        torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / 1e3 / steps
+
+
+def run_native(args, ws, rank, local):
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    hbm, tf_burst, tf_sus, peak_kind = peaks()
+    spec, _ = synth.workload(WORKLOAD)
+    M = 1
+    hs, _ = make_layers(spec, LAYERS)
+    xs = [synth.make_x(M, spec.K, spec.dtype, seed=100 + i).cuda() for i in range(LAYERS)]
+    ys = [torch.empty(M, spec.N, dtype=torch.bfloat16, device="cuda") for _ in range(LAYERS)]
+    launches_per_call = gptq.gptq_gemm_launches(hs[0], M)
+
+    def measure():
+        barrier(ws)
+        torch.cuda.synchronize()
+        total = time_calls(hs, xs, ys, M, args.steps, args.warmup, graph=True)
+        barrier(ws)
+        eager = time_calls(hs, xs, ys, M, args.steps, args.warmup, graph=False)
+        barrier(ws)
+        return max_over_ranks(ws, total), max_over_ranks(ws, eager)
+
+    with ClockSampler(local) as clk:
+        total, eager = measure()
+        # end to end through the public API with host buffers
+        xh = [synth.make_x(M, spec.K, spec.dtype, seed=100 + i).pin_memory() for i in range(LAYERS)]
+        yh = [torch.empty(M, spec.N, dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
+        st = torch.cuda.current_stream()
+        for i in range(args.warmup):
+            xs[i % LAYERS].copy_(xh[i % LAYERS], non_blocking=True)
+            gptq.gptq_gemm(hs[i % LAYERS], xs[i % LAYERS], ys[i % LAYERS], M, st)
+            yh[i % LAYERS].copy_(ys[i % LAYERS], non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for i in range(args.steps):
+            xs[i % LAYERS].copy_(xh[i % LAYERS], non_blocking=True)
+            gptq.gptq_gemm(hs[i % LAYERS], xs[i % LAYERS], ys[i % LAYERS], M, st)
+            yh[i % LAYERS].copy_(ys[i % LAYERS], non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize()
+        e2e_t = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3 / args.steps)
+        barrier(ws)
+        extra = {} if (args.no_extra or rank != 0) else extra_workloads(args, hbm, tf_burst, peak_kind)
+    clocks = clk.summary()
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(clocks["reasons"])
+    if bad and not args._remeasured:
+        args._remeasured = True
+        total, eager = measure()
+
+    B = b_alg(spec, M)
+    value = B * ws / total / 1e9
+    achieved = B / total / 1e9
+    traffic = traffic_record("gemm_small.cu")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total * 1e3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "us_per_call": round(total * 1e6, 3),
+        "config": {"workload": WORKLOAD, "M": M, "K": spec.K, "N": spec.N, "bits": spec.bits,
+                   "group_size": spec.group_size, "zero": "symmetric 8", "act_dtype": "bf16",
+                   "layers_rotated": LAYERS, "l2": f"inputs larger than L2: {LAYERS} resident weight sets "
+                   f"({LAYERS * B / 1e6:.0f} MB) rotated per step", "parallelism": f"replicas x{ws}",
+                   "bytes_per_call": B},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+                     "kernel": "k_gemm_small (small-M, mma.sync swap-AB, cluster split-K)",
+                     "timing": "CUDA events around one replay of a graph of the timed calls"},
+        "eager_us_per_call": round(eager * 1e6, 3),
+        "e2e": {"value": round(B * ws / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": 2 * M * spec.K,
+                "d2h_bytes_per_step": 2 * M * spec.N, "us_per_step": round(e2e_t * 1e6, 3)},
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, calls, secs, cores, sample = oracle_sample_rate(spec, M, args.cpu_seconds, 2048)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if extra:
+        line["detail"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for h in hs:
+        h.close()
+    return 0
+
+
+def extra_workloads(args, hbm, tf_burst, peak_kind):
+    """Rank 0: the other M values of the decode layer, the 70B gate layer, and prefill."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    out = {}
+    steps = max(20, min(args.steps, 200))
+
+    def one(name, spec, Ms, layers):
+        hs, _ = make_layers(spec, layers, seed0=1000)
+        Mmax = max(Ms)
+        for h in hs:
+            gptq.gptq_reserve(h, Mmax)
+        res = {}
+        for M in Ms:
+            xs = [synth.make_x(M, spec.K, spec.dtype, seed=M + i).cuda() for i in range(min(layers, 4))]
+            dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
+            ys = [torch.empty(M, spec.N, dtype=dt, device="cuda") for _ in range(min(layers, 4))]
+            n = steps if M <= 64 else max(5, steps // 10)
+            launch = time_calls(hs, xs, ys, M, n, 3, graph=True)
+            B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
+            roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
+            res[f"M={M}"] = {"us": round(launch * 1e6, 2), "GB/s": round(B / launch / 1e9, 1),
+                             "TFLOP/s": round(F / launch / 1e12, 2), "roofline_frac": round(roof / launch, 4),
+                             "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+            del xs, ys
+        for h in hs:
+            h.close()
+        torch.cuda.empty_cache()
+        out[name] = res
+
+    s2, _ = synth.workload(WORKLOAD)
+    one(WORKLOAD, s2, [8, 16], LAYERS)
+    s3, m3 = synth.workload("llama3-70b-gate-8192x28672-b4g128-descact")
+    one("llama3-70b-gate-8192x28672-b4g128-descact", s3, m3, 4)
+    s4, m4 = synth.workload("prefill-8192x28672-b4g128")
+    one("prefill-8192x28672-b4g128", s4, [4096] if args.quick_prefill else m4, 1)
+    out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "kind": peak_kind}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other layers and M values")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--quick-prefill", action="store_true", help="prefill at M=4096 only")
+    args = ap.parse_args()
+    args._remeasured = False
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        return run_reference(args, ws, rank)
+    ws, rank, local = dist_setup()
+    try:
+        return run_native(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -164,6 +164,12 @@ gptq_status_t gptq_get_info(gptq_handle_t h, gptq_info_t* info);
 gptq_status_t gptq_copy_runtime(gptq_handle_t h, void* wr, int32_t* perm, int32_t* cgid,
                                 void* s_r, uint8_t* z_r);
 
+/* GPTQ_ERR_TIMEOUT if a kernel launched with this handle gave up a bounded device-side wait (an
+ * mbarrier wait that exceeded its time limit; the kernel then skipped its remaining work and the
+ * outputs of that call are invalid) since the previous call of this function, else GPTQ_OK.  Clears
+ * the record.  Synchronizes the handle's device.  Errors: INVALID_ARG, CUDA. */
+gptq_status_t gptq_device_status(gptq_handle_t h);
+
 /* Static text for a status. */
 const char* gptq_status_string(gptq_status_t s);
 

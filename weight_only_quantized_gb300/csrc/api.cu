@@ -41,6 +41,7 @@ static void free_handle(Handle* h) {
   cudaFree(h->s_r);
   cudaFree(h->z_r);
   cudaFree(h->xp);
+  cudaFree(h->err);
   delete h;
 }
 
@@ -177,6 +178,9 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
   h->K = K; h->N = N; h->bits = bits; h->group_size = group_size; h->G = G;
   h->Np = (N + 255) / 256 * 256;
   h->dtype = dtype;
+  cudaError_t ce = cudaMalloc(&h->err, sizeof(int32_t));
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(h->err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaMalloc(error word)"); }
   s = build_runtime(*h, qweight, qzeros, scales, g_idx, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
@@ -231,6 +235,19 @@ gptq_status_t gptq_destroy(gptq_handle_t hh) {
   free_handle(h);
   if (cur >= 0 && cur != dev) cudaSetDevice(cur);
   if (e != cudaSuccess) return cuda_fail(e, "gptq_destroy: cudaDeviceSynchronize");
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_device_status(gptq_handle_t hh) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  Handle& h = *reinterpret_cast<Handle*>(hh);
+  int32_t word = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&word, h.err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != DEV_ERR_NONE) e = cudaMemset(h.err, 0, sizeof(int32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "gptq_device_status");
+  if (word == DEV_ERR_TIMEOUT)
+    return fail(GPTQ_ERR_TIMEOUT, "a kernel gave up a bounded wait on an mbarrier; that call's output is invalid");
   return GPTQ_OK;
 }
 

@@ -6,7 +6,10 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cstddef>
+#include <mutex>
 #include <string>
+#include <unordered_map>
+#include <vector>
 
 #include "../../include/gptq.h"
 
@@ -27,11 +30,16 @@ struct Handle {
   int32_t* cgid = nullptr;   // [Kr/32] group of each 32-row chunk
   uint16_t* s_r = nullptr;   // [G][Np] scale bits
   uint8_t* z_r = nullptr;    // [G][Np] stored zero (zero - 1)
+  std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)
+  int32_t* err = nullptr;    // device error word: kernels set it when a bounded wait gives up
   // workspace
   int reserved_M = 0;
   void* xp = nullptr;        // [reserved_M][Kr] activations in sorted order (large-M path)
   size_t xp_bytes = 0;
   size_t wr_bytes() const { return (size_t)Kr / 128 * bits * Np * 16; }
+  // Launch plans by (path, M): computed once, so a call costs one kernel launch on the host.
+  mutable std::mutex plan_mu;
+  mutable std::unordered_map<int64_t, std::vector<int64_t>> plans;
 };
 
 // Status with message, recorded per thread.
@@ -39,8 +47,6 @@ gptq_status_t fail(gptq_status_t s, const std::string& msg);
 gptq_status_t cuda_fail(cudaError_t e, const char* what);
 
 // ---- kernels launched from the host code (defined in the .cu files) ----
-cudaError_t launch_repack(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                          const int32_t* g_idx, cudaStream_t st, int* err_host_flags);
 
 // Small-M path: mma.sync (swap-AB) kernel with split-K reduced inside a thread-block cluster.
 int small_m_launches(const Handle& h, int M);
@@ -71,6 +77,47 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Device error codes written to Handle::err (0 = none).
+enum : int32_t { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1 };
+
+// ---- mbarrier and bulk-copy helpers (sm_90+ PTX) ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with the given parity to complete; give up after limit_ns (returns false).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+// Bulk copy global -> this CTA's shared memory, completing tx bytes on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 }  // namespace gptq

@@ -251,7 +251,12 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
   k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, h.s_r, h.z_r);
   if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
-  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack"); }
+  h.cgid_host.resize(h.Kr / 32);
+  if ((e = cudaMemcpyAsync(h.cgid_host.data(), h.cgid, sizeof(int32_t) * (h.Kr / 32), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "repack");
+  }
   cleanup();
   return GPTQ_OK;
 }

@@ -45,6 +45,7 @@ SIGNATURES = {
     "gptq_destroy": (_I, [_P]),
     "gptq_get_info": (_I, [_P, C.POINTER(GptqInfo)]),
     "gptq_copy_runtime": (_I, [_P, _P, _P, _P, _P, _P]),
+    "gptq_device_status": (_I, [_P]),
     "gptq_status_string": (C.c_char_p, [_I]),
     "gptq_last_error_message": (C.c_char_p, []),
 }
@@ -167,6 +168,11 @@ def gptq_gemm_launches(h: Handle, M: int, path: int = PATH_AUTO) -> int:
 
 def gptq_destroy(h: Handle):
     h.close()
+
+
+def gptq_device_status(h: Handle):
+    """Raise GptqError(GPTQ_ERR_TIMEOUT) if a kernel of this handle gave up a bounded wait."""
+    _check(lib().gptq_device_status(h.ptr))
 
 
 def gptq_get_info(h: Handle) -> GptqInfo:
