@@ -170,6 +170,34 @@ gptq_status_t gptq_copy_runtime(gptq_handle_t h, void* wr, int32_t* perm, int32_
  * the record.  Synchronizes the handle's device.  Errors: INVALID_ARG, CUDA. */
 gptq_status_t gptq_device_status(gptq_handle_t h);
 
+/*
+ * Repack into caller-owned device buffers without allocating anything (no cudaMalloc, no
+ * cudaFree, no allocating library call).  The pages have no counterpart of this call: it exists
+ * for callers that cannot allocate device memory themselves at load time -- a server that carves
+ * every weight out of one arena reserved up front, or a host framework that owns the device
+ * allocator and forbids other allocations -- and that still want the runtime layout.
+ *   qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype: as for gptq_repack.
+ *   wr          device, wr_capacity bytes, 16-byte aligned: receives the packed codes.
+ *   perm, cgid  device, int32 [kr_capacity] and [kr_capacity/32], 16-byte aligned.
+ *   s_r, z_r    device, scale bits [G, N_padded] and stored zeros [G, N_padded], N_padded =
+ *               roundup(N, 256).
+ *   k_sorted    host, receives K_sorted (set before the capacity check, so a caller can retry).
+ * The outputs are exactly what gptq_copy_runtime reports for a handle built from the same
+ * checkpoint.  kr_capacity = roundup(K + 31*G, 128) and wr_capacity = kr_capacity/128*bits*
+ * N_padded*16 always suffice.  Its scratch is a fixed array of 3*4096+8 int32 in device memory
+ * that every GPU holds once the library is loaded, so a layer may have at most 4096 groups
+ * (GPTQ_ERR_UNSUPPORTED above that).  The first call on a device looks up that array's device
+ * address.  Every call on a device shares the array, so calls that overlap on the same GPU race;
+ * the call synchronizes `stream` once to read the g_idx histogram.
+ * Errors: INVALID_ARG, UNSUPPORTED, SHAPE, ALIGNMENT, DEVICE, INVALID_GIDX, WORKSPACE (output
+ * buffers too small for the sorted K), CUDA.
+ */
+gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                                  const int32_t* g_idx, int K, int N, int bits, int group_size,
+                                  gptq_dtype_t dtype, void* wr, size_t wr_capacity, int32_t* perm,
+                                  int32_t* cgid, int kr_capacity, void* s_r, uint8_t* z_r,
+                                  int* k_sorted, void* stream);
+
 /* Static text for a status. */
 const char* gptq_status_string(gptq_status_t s);
 

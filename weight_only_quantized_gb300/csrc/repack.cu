@@ -261,4 +261,104 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   return GPTQ_OK;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free repack (gptq_repack_noalloc).  Its only scratch, the per-group counts, offsets
+// and cursors of the sort plus a few flags, lives in this file-scope device array, which every
+// device that loads the library holds until the process exits.  In host code the array's name is
+// a host-side stand-in, so its device address is looked up once per device with
+// cudaGetSymbolAddress (on the first call made with that device current) and passed to the
+// kernels.  All calls on a device share the array: the counts are cleared by k_histogram and the
+// cursors by a memset on every call, and calls that overlap on the same GPU (for example on two
+// streams) race on it.
+constexpr int kNoallocMaxGroups = 4096;
+static __device__ __align__(256) int32_t g_noalloc_scratch[3 * kNoallocMaxGroups + M_N];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on the first call there).
+cudaError_t noalloc_scratch(int dev, int32_t** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
 }  // namespace gptq
+
+extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                                             const int32_t* g_idx, int K, int N, int bits, int group_size,
+                                             gptq_dtype_t dtype, void* wr, size_t wr_capacity, int32_t* perm,
+                                             int32_t* cgid, int kr_capacity, void* s_r, uint8_t* z_r,
+                                             int* k_sorted, void* stream) {
+  using namespace gptq;
+  if (k_sorted) *k_sorted = 0;
+  if (!qweight || !qzeros || !scales || !wr || !perm || !cgid || !s_r || !z_r || !k_sorted)
+    return fail(GPTQ_ERR_INVALID_ARG, "gptq_repack_noalloc: every input and output buffer is required");
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 8)
+    return fail(GPTQ_ERR_UNSUPPORTED, "GPTQ-001: bits must be 2, 3, 4 or 8, got " + std::to_string(bits));
+  if (dtype != GPTQ_FP16 && dtype != GPTQ_BF16) return fail(GPTQ_ERR_UNSUPPORTED, "dtype must be GPTQ_FP16 or GPTQ_BF16");
+  if (group_size != -1 && group_size < 1) return fail(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or >= 1");
+  if (K < 32 || K % 32 != 0 || K > (1 << 17)) return fail(GPTQ_ERR_SHAPE, "GPTQ-002: in_features must be a multiple of 32 in [32, 131072]");
+  if (N < 32 || N % 32 != 0 || N > (1 << 18)) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a multiple of 32 in [32, 262144]");
+  const int G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
+  if (G > kNoallocMaxGroups)
+    return fail(GPTQ_ERR_UNSUPPORTED, "gptq_repack_noalloc: at most " + std::to_string(kNoallocMaxGroups) +
+                                          " groups (its fixed scratch); this layer has " + std::to_string(G));
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(wr) | reinterpret_cast<uintptr_t>(perm) | reinterpret_cast<uintptr_t>(cgid);
+  if ((a16 & 15) || (reinterpret_cast<uintptr_t>(qweight) & 3) || (reinterpret_cast<uintptr_t>(qzeros) & 3) ||
+      (reinterpret_cast<uintptr_t>(scales) & 1) || (reinterpret_cast<uintptr_t>(s_r) & 1) ||
+      (g_idx && (reinterpret_cast<uintptr_t>(g_idx) & 3)))
+    return fail(GPTQ_ERR_ALIGNMENT, "wr, perm and cgid need 16-byte alignment; qweight, qzeros, g_idx 4; scales, s_r 2");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(GPTQ_ERR_DEVICE, "device ordinal out of range");
+  int major = 0, minor = 0;
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3) return fail(GPTQ_ERR_DEVICE, "this library is built for sm_103a (compute capability 10.3)");
+  int32_t* scratch = nullptr;
+  if ((e = noalloc_scratch(dev, &scratch)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(repack scratch)");
+  int32_t* cnt = scratch;
+  int32_t* off = scratch + G;
+  int32_t* cursor = scratch + 2 * G;
+  int32_t* meta = scratch + 3 * kNoallocMaxGroups;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int Np = (N + 255) / 256 * 256;
+
+  int32_t meta_h[M_N] = {};
+  k_histogram<<<1, 1024, 0, st>>>(g_idx, K, G, group_size, cnt, off, meta);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "histogram launch");
+  if ((e = cudaMemcpyAsync(meta_h, meta, sizeof(meta_h), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return cuda_fail(e, "repack: reading the g_idx histogram");
+  if (meta_h[M_BAD_GIDX])
+    return fail(GPTQ_ERR_INVALID_GIDX, "GPTQ-004: g_idx[" + std::to_string(meta_h[M_BAD_K]) + "] selects no scale/zero row");
+  const int Kr = meta_h[M_KR], Ks = meta_h[M_KS], last_g = meta_h[M_LAST_G];
+  *k_sorted = Kr;
+  const size_t wr_b = (size_t)Kr / 128 * bits * Np * 16;
+  if (Kr > kr_capacity || wr_b > wr_capacity)
+    return fail(GPTQ_ERR_WORKSPACE, "gptq_repack_noalloc: the sorted K is " + std::to_string(Kr) + " rows (" +
+                                        std::to_string(wr_b) + " code bytes); the output buffers are smaller");
+  if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * G, st)) != cudaSuccess) return cuda_fail(e, "memset");
+  k_scatter_perm<<<1, 32, 0, st>>>(g_idx, K, group_size, off, cursor, perm);
+  k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, Kr, last_g, cnt, off, perm, cgid);
+  const int nBV = (Kr / 128) * bits;
+  dim3 gc(Np / 256, nBV < 65535 ? nBV : 65535);
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, N, Np, bits, nBV, static_cast<uint8_t*>(wr));
+  dim3 gs(Np / 256, G < 65535 ? G : 65535);
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, Np, bits, G,
+                                static_cast<uint16_t*>(s_r), z_r);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "repack launch");
+  return GPTQ_OK;
+}

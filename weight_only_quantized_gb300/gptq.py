@@ -46,6 +46,7 @@ SIGNATURES = {
     "gptq_get_info": (_I, [_P, C.POINTER(GptqInfo)]),
     "gptq_copy_runtime": (_I, [_P, _P, _P, _P, _P, _P]),
     "gptq_device_status": (_I, [_P]),
+    "gptq_repack_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P, _I, _P, _P, _P, _P]),
     "gptq_status_string": (C.c_char_p, [_I]),
     "gptq_last_error_message": (C.c_char_p, []),
 }
@@ -173,6 +174,25 @@ def gptq_destroy(h: Handle):
 def gptq_device_status(h: Handle):
     """Raise GptqError(GPTQ_ERR_TIMEOUT) if a kernel of this handle gave up a bounded wait."""
     _check(lib().gptq_device_status(h.ptr))
+
+
+def gptq_repack_noalloc(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+                        g_idx: Optional[torch.Tensor], bits: int, group_size: int, wr: torch.Tensor,
+                        perm: torch.Tensor, cgid: torch.Tensor, s_r: torch.Tensor, z_r: torch.Tensor,
+                        stream=None) -> int:
+    """Repack into caller-owned device tensors; the library allocates nothing.  Returns K_sorted.
+
+    wr: uint8 (capacity = numel), perm: int32 [kr_capacity], cgid: int32 [kr_capacity // 32],
+    s_r: fp16/bf16-sized 2-byte [G, N_padded], z_r: uint8 [G, N_padded]."""
+    K, N = gptq_check_shapes(bits, tuple(qweight.shape), tuple(qzeros.shape), tuple(scales.shape),
+                             0 if g_idx is None else g_idx.numel(), group_size)
+    if scales.dtype not in DTYPE:
+        raise GptqError(2, "scales must be fp16 or bf16")
+    kr = C.c_int()
+    _check(lib().gptq_repack_noalloc(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
+                                     DTYPE[scales.dtype], _ptr(wr), wr.numel() * wr.element_size(), _ptr(perm),
+                                     _ptr(cgid), perm.numel(), _ptr(s_r), _ptr(z_r), C.byref(kr), _stream(stream)))
+    return kr.value
 
 
 def gptq_get_info(h: Handle) -> GptqInfo:
