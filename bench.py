@@ -394,6 +394,31 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
     return out
 
 
+PROFILE_LAYERS = {"decode": WORKLOAD, "gate": "llama3-70b-gate-8192x28672-b4g128-descact",
+                  "prefill": "prefill-8192x28672-b4g128"}
+
+
+def run_profile(args):
+    """One layer, one weight set, `steps` eager calls at M = --profile-m: a small, fixed launch
+    sequence for ncu captures (repack kernels first, then warm-up and timed gptq_gemm launches)."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    spec, _ = synth.workload(PROFILE_LAYERS[args.profile_layer])
+    M = args.profile_m
+    hs, _ = make_layers(spec, 1)
+    gptq.gptq_reserve(hs[0], M)
+    dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
+    xs = [synth.make_x(M, spec.K, spec.dtype, seed=3).cuda()]
+    ys = [torch.empty(M, spec.N, dtype=dt, device="cuda")]
+    t = time_calls(hs, xs, ys, M, args.steps, args.warmup, graph=False)
+    B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
+    print(json.dumps({"profile_layer": args.profile_layer, "M": M, "us_per_call": round(t * 1e6, 2),
+                      "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),
+                      "launches_per_call": gptq.gptq_gemm_launches(hs[0], M)}), flush=True)
+    hs[0].close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,6 +429,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--quick-prefill", action="store_true", help="prefill at M=4096 only")
+    ap.add_argument("--profile-layer", choices=["decode", "gate", "prefill"], default=None,
+                    help="profiling mode: time only this layer at --profile-m (one weight set) and print one line")
+    ap.add_argument("--profile-m", type=int, default=1)
     args = ap.parse_args()
     args._remeasured = False
     if args.warmup < 3:
@@ -413,6 +441,8 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         return run_reference(args, ws, rank)
     ws, rank, local = dist_setup()
+    if args.profile_layer:
+        return run_profile(args)
     try:
         return run_native(args, ws, rank, local)
     finally:

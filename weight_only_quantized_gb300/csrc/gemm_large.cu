@@ -16,7 +16,7 @@
 //  * warp 0: producer.  cp.async.bulk copies of the packed 128-row blocks of the tile's 128
 //    columns, and TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of 256 x 64 x tiles, each into
 //    a ring tracked by mbarriers.
-//  * warps 2..5: dequantisers.  Thread d owns weight row n0 + d: one LOP3 per code pair makes
+//  * warps 2..3: dequantisers.  Thread d owns weight rows n0 + d and n0 + d + 64: one LOP3 per code pair makes
 //    magic + code, one packed subtract of (magic + zero) leaves the exact integer code - zero, and
 //    the row is written in the UMMA K-major SWIZZLE_128B layout (16-byte chunk j of row r at chunk
 //    j ^ (r % 8) of its 128-byte row), then a generic-to-async proxy fence and an arrive.
@@ -24,7 +24,7 @@
 //    tcgen05.mma.cta_group::1.kind::f16 (M = 128 weight rows, N = 256 x rows, K = 16), two per
 //    32-row chunk, restarting the accumulator at each group and committing the buffer when the
 //    group ends.
-//  * warps 6..21: sixteen scaler warps, four per TMEM lane quarter, 64 columns each.  Per group:
+//  * warps 4..19: sixteen scaler warps, four per TMEM lane quarter, 64 columns each.  Per group:
 //    tcgen05.ld the partial sums, S += scale[g][n] * P in registers, release the buffer.  At the end
 //    they round S to the output type and store y.
 // Act-order handles first gather x into the handle's workspace in sorted k order (one extra launch).
@@ -38,9 +38,9 @@ namespace gptq {
 namespace {
 
 constexpr int BN = 128, BMX = 256, HK = 64;   // weight rows (MMA M), x rows (MMA N), k per stage
-constexpr int kDqWarps = 4, kScWarps = 16;
+constexpr int kDqWarps = 2, kScWarps = 16;
 constexpr int kWarpsL = 2 + kDqWarps + kScWarps;
-constexpr int kThreadsL = kWarpsL * 32;         // 704
+constexpr int kThreadsL = kWarpsL * 32;         // 640: up to 96 registers a thread, so the scalers' sums stay in registers
 constexpr int PS = 2, XS = 3, WS = 3;
 constexpr int X_BYTES = BMX * HK * 2;           // 32 KB
 constexpr int W_BYTES = BN * HK * 2;            // 16 KB
@@ -164,12 +164,10 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
 
-// 16 consecutive fp32 columns of this warp's TMEM lane quarter.
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-               "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+// 8 consecutive fp32 columns of this warp's TMEM lane quarter.
+__device__ __forceinline__ void tmem_ld8(uint32_t addr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(addr));
 }
 
@@ -286,51 +284,59 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
     }
   } else if (warp < 2 + kDqWarps) {
-    // ---------------- dequantisers: thread d owns weight row n0 + d ----------------
-    const int d = tid - 64;
-    const int n = n0 + d;
-    uint32_t zq[4];
-    auto load_zeros = [&](int blk, uint32_t (&z)[4]) {
+    // ---------------- dequantisers: thread d owns weight rows n0 + d + 64 r, r = 0, 1 ----------------
+    const int d0 = tid - 64;
+    uint32_t zq[2][4];
+    auto load_zeros = [&](int blk, uint32_t (&z)[2][4]) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) z[c] = prep_zero_l<T, BITS>(__ldg(&a.z_r[(size_t)cg[blk * 4 + c] * a.Np + n]));
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          z[r][c] = prep_zero_l<T, BITS>(__ldg(&a.z_r[(size_t)cg[blk * 4 + c] * a.Np + n0 + d0 + 64 * r]));
     };
     if (nblocks > 0) load_zeros(0, zq);
     for (int blk = 0; blk < nblocks && ok; ++blk) {
       const int ps = blk % PS;
       if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
       const uint8_t* stage = pk + ps * PKB;
-      Words<BITS> lw[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) stage_words<BITS>(lw[t], stage, d, t);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pk_empty(ps));
-      uint32_t zn[4];
+      uint32_t zn[2][4];
       if (blk + 1 < nblocks) load_zeros(blk + 1, zn);     // next block's zeros, ahead of use
       for (int h = 0; h < 2; ++h) {
         const int i = 2 * blk + h, ws = i % WS;
         if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
-        uint8_t* row = base + S::w + ws * W_BYTES + d * 128;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * h + cc;
+        for (int r = 0; r < 2; ++r) {
+          const int d = d0 + 64 * r;
+          Words<BITS> lw[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint4 o;
-            o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[c]);
-            o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[c]);
-            o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[c]);
-            o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[c]);
-            const int j = 4 * cc + t;                       // 16-byte chunk (8 k) inside the 64-k row
-            *reinterpret_cast<uint4*>(row + ((j ^ (d & 7)) << 4)) = o;
+          for (int t = 0; t < 4; ++t) stage_words<BITS>(lw[t], stage, d, t);
+          uint8_t* row = base + S::w + ws * W_BYTES + d * 128;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * h + cc;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint4 o;
+              o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[r][c]);
+              o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[r][c]);
+              o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[r][c]);
+              o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[r][c]);
+              const int j = 4 * cc + t;                       // 16-byte chunk (8 k) inside the 64-k row
+              *reinterpret_cast<uint4*>(row + ((j ^ (d & 7)) << 4)) = o;
+            }
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(w_full(ws));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pk_empty(ps));           // both halves of this block are written
       if (blk + 1 < nblocks) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) zq[c] = zn[c];
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) zq[r][c] = zn[r][c];
       }
     }
     if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
@@ -360,12 +366,12 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256 + 64 * cs);
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        uint32_t r[16];
-        tmem_ld16(taddr + 16 * part, r);
+      for (int part = 0; part < 8; ++part) {
+        uint32_t r[8];
+        tmem_ld8(taddr + 8 * part, r);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[16 * part + j] = fmaf(sc, __uint_as_float(r[j]), acc[16 * part + j]);
+        for (int j = 0; j < 8; ++j) acc[8 * part + j] = fmaf(sc, __uint_as_float(r[j]), acc[8 * part + j]);
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
