@@ -16,17 +16,19 @@
 //  * warp 0: producer.  cp.async.bulk copies of the packed 128-row blocks of the tile's 128
 //    columns, and TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of 256 x 64 x tiles, each into
 //    a ring tracked by mbarriers.
-//  * warps 2..3: dequantisers.  Thread d owns weight rows n0 + d and n0 + d + 64: one LOP3 per code pair makes
-//    magic + code, one packed subtract of (magic + zero) leaves the exact integer code - zero, and
-//    the row is written in the UMMA K-major SWIZZLE_128B layout (16-byte chunk j of row r at chunk
-//    j ^ (r % 8) of its 128-byte row), then a generic-to-async proxy fence and an arrive.
-//  * warp 1: allocates all 512 TMEM columns (two 256-column partial-sum buffers); one thread issues
-//    tcgen05.mma.cta_group::1.kind::f16 (M = 128 weight rows, N = 256 x rows, K = 16), two per
-//    32-row chunk, restarting the accumulator at each group and committing the buffer when the
-//    group ends.
-//  * warps 4..19: sixteen scaler warps, four per TMEM lane quarter, 64 columns each.  Per group:
-//    tcgen05.ld the partial sums, S += scale[g][n] * P in registers, release the buffer.  At the end
-//    they round S to the output type and store y.
+//  * warps 4..7: dequantisers, one per SM sub-partition.  Thread d owns weight row n0 + d: one LOP3
+//    per code pair makes magic + code, one packed subtract of (magic + zero) leaves the exact
+//    integer code - zero, and the row is written in the UMMA K-major SWIZZLE_128B layout (16-byte
+//    chunk j of row r at chunk j ^ (r % 8) of its 128-byte row), then a generic-to-async proxy
+//    fence and an arrive.
+//  * warp 1: allocates all 512 TMEM columns (two 256-column partial-sum buffers); the warp runs
+//    the schedule and one elected lane issues tcgen05.mma.cta_group::1.kind::f16 (M = 128 weight
+//    rows, N = 256 x rows, K = 16), two per 32-row chunk, restarting the accumulator at each group
+//    and committing the buffer when the group ends.
+//  * warps 8..15: eight scaler warps, two per TMEM lane quarter, 128 columns each.  Per group:
+//    tcgen05.ld the partial sums (16 columns in flight while the previous 16 are used),
+//    S += scale[g][n] * P in registers, release the buffer.  At the end they round S to the output
+//    type and store y.  setmaxnreg gives them 184 registers a thread and the other warps 72.
 // Act-order handles first gather x into the handle's workspace in sorted k order (one extra launch).
 // Every wait is bounded; a timeout sets the handle's error word and the CTA drains and exits.
 #include "internal.cuh"
@@ -38,13 +40,19 @@ namespace gptq {
 namespace {
 
 constexpr int BN = 128, BMX = 256, HK = 64;   // weight rows (MMA M), x rows (MMA N), k per stage
-constexpr int kDqWarps = 2, kScWarps = 16;
-constexpr int kWarpsL = 2 + kDqWarps + kScWarps;
-constexpr int kThreadsL = kWarpsL * 32;         // 640: up to 96 registers a thread, so the scalers' sums stay in registers
+// Four warpgroups: {producer, MMA issuer, two spare}, four dequantisers (one per SM sub-partition),
+// and eight scalers (two per TMEM lane quarter, 128 fp32 sums a thread).  setmaxnreg moves
+// registers from the first two warpgroups to the scalers: 2 x 128 x (72 + 184) = 65536.
+constexpr int kDqWarps = 4, kScWarps = 8;
+constexpr int kDqWarp0 = 4, kScWarp0 = 8;
+constexpr int kThreadsL = 512;
+constexpr int kRegsLaunch = 128, kRegsLight = 72, kRegsScaler = 184;
+static_assert(2 * 128 * (kRegsLight + kRegsScaler) <= kThreadsL * kRegsLaunch, "register split exceeds the launch");
 constexpr int PS = 2, XS = 3, WS = 3;
 constexpr int X_BYTES = BMX * HK * 2;           // 32 KB
 constexpr int W_BYTES = BN * HK * 2;            // 16 KB
 constexpr int kTmemCols = 512;                  // two partial-sum buffers of 256 columns
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 template <int BITS> constexpr int PK_BYTES = BN * 16 * BITS;  // one 128-row block of 128 columns
 
 template <typename T> struct MagicL;
@@ -58,9 +66,10 @@ template <int BITS> struct LargeSmem {
   static constexpr int w = x + XS * X_BYTES;
   static constexpr int pk = w + WS * W_BYTES;
   static constexpr int bars = pk + PS * PK_BYTES<BITS>;
-  static constexpr int nbars = 2 * XS + 2 * WS + 2 * PS + 4;
+  static constexpr int nbars = 2 * XS + 2 * WS + 2 * PS + 5;
   static constexpr int tmem_slot = bars + nbars * 8;
-  static constexpr int cg = tmem_slot + 16;       // int32 chunk groups of the whole K follow
+  static constexpr int cg = tmem_slot + 16;       // int32 group of every 32-row chunk, then one
+                                                  // uint32 group-end mask per 32 chunks
 };
 
 struct LargeArgs {
@@ -106,6 +115,25 @@ __device__ __forceinline__ void stage_words(Words<BITS>& o, const uint8_t* stage
   } else {
     const uint2 v = *reinterpret_cast<const uint2*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1));
     o.w[0] = v.x; o.w[1] = v.y;
+    o.w[2] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)2 * BN + d) * 16 + 4 * t);
+  }
+}
+
+// The words of lane t that chunks 2h and 2h + 1 of a 128-row block use (other entries untouched):
+// 4-bit: word c of vector t; 2-bit: word c/2; 8-bit: words 2c, 2c+1 (vector 2t + h); 3-bit: word
+// c/2 of the 2-bit plane and the lane's word of the 1-bit plane.
+template <int BITS>
+__device__ __forceinline__ void half_words(Words<BITS>& o, const uint8_t* stage, int d, int t, int h) {
+  if constexpr (BITS == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(stage + ((size_t)t * BN + d) * 16 + 8 * h);
+    o.w[2 * h] = v.x; o.w[2 * h + 1] = v.y;
+  } else if constexpr (BITS == 2) {
+    o.w[h] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1) + 4 * h);
+  } else if constexpr (BITS == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + ((size_t)(2 * t + h) * BN + d) * 16);
+    o.w[4 * h] = v.x; o.w[4 * h + 1] = v.y; o.w[4 * h + 2] = v.z; o.w[4 * h + 3] = v.w;
+  } else {
+    o.w[h] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1) + 4 * h);
     o.w[2] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)2 * BN + d) * 16 + 4 * t);
   }
 }
@@ -163,14 +191,39 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
 }
-
-// 8 consecutive fp32 columns of this warp's TMEM lane quarter.
-__device__ __forceinline__ void tmem_ld8(uint32_t addr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(addr));
+// Commit only when pred != 0 (a predicated instruction, no branch).
+__device__ __forceinline__ void umma_commit_if(uint32_t bar, uint32_t pred) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+               "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+               :: "r"(bar), "r"(pred) : "memory");
+}
+// tcgen05.mma issued only by the lane with go != 0.
+__device__ __forceinline__ void umma_f16_if(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc, uint32_t go) {
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+               "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(go) : "memory");
+}
+// 1 in exactly one lane of the (converged) warp.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred;
 }
 
+// 16 consecutive fp32 columns of this warp's TMEM lane quarter; the wait names the registers so
+// no use of them can be scheduled above it.
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(addr));
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :: "memory");
+}
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, const __grid_constant__ CUtensorMap tmap_x) {
   using S = LargeSmem<BITS>;
@@ -196,8 +249,11 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   auto pk_empty = [&](int i) { return bar + 8 * (2 * XS + 2 * WS + PS + i); };
   auto p_full = [&](int b) { return bar + 8 * (2 * XS + 2 * WS + 2 * PS + b); };
   auto p_empty = [&](int b) { return bar + 8 * (2 * XS + 2 * WS + 2 * PS + 2 + b); };
+  const uint32_t mma_done = bar + 8 * (2 * XS + 2 * WS + 2 * PS + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + S::tmem_slot);
   int32_t* cg = reinterpret_cast<int32_t*>(base + S::cg);
+  uint32_t* gmask = reinterpret_cast<uint32_t*>(base + S::cg + 4 * nchunks);
+  const int nwin = (nchunks + 31) / 32;
   // a 32-row chunk c ends its group when the next chunk has another group (or c is the last)
   auto group_ends = [&](int c) { return c + 1 == nchunks || cg[c + 1] != cg[c]; };
 
@@ -206,6 +262,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     for (int i = 0; i < WS; ++i) { mbar_init(w_full(i), kDqWarps); mbar_init(w_empty(i), 1); }
     for (int i = 0; i < PS; ++i) { mbar_init(pk_full(i), 1); mbar_init(pk_empty(i), kDqWarps); }
     for (int b = 0; b < 2; ++b) { mbar_init(p_full(b), 1); mbar_init(p_empty(b), kScWarps); }
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -214,6 +271,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   for (int i = tid; i < nchunks; i += kThreadsL) cg[i] = __ldg(&a.cgid[i]);
+  // bit j of gmask[w]: chunk 32 w + j is the last chunk of its group (the MMA issuer's schedule)
+  for (int w0 = 32 * warp; w0 < nchunks; w0 += kThreadsL) {
+    const int c = w0 + lane;
+    const bool end = c < nchunks && (c + 1 == nchunks || __ldg(&a.cgid[c + 1]) != __ldg(&a.cgid[c]));
+    const uint32_t m = __ballot_sync(0xffffffffu, end);
+    if (lane == 0) gmask[w0 / 32] = m;
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -221,157 +285,43 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   bool ok = true;
-  if (warp == 0) {
-    // ---------------- producer ----------------
-    if (lane == 0) {
-      int pk_issued = 0, x_issued = 0;
-      for (int blk = 0; blk < nblocks && ok; ++blk) {
-        const int ps = blk % PS;
-        if (blk >= PS && !mbar_wait(pk_empty(ps), ((blk / PS) - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(pk_full(ps), PKB);
-        const uint8_t* src = a.wr + ((size_t)blk * BITS * a.Np + n0) * 16;
-#pragma unroll
-        for (int v = 0; v < BITS; ++v)
-          bulk_g2s(smem_u32(pk + ps * PKB + v * BN * 16), src + (size_t)v * a.Np * 16, BN * 16, pk_full(ps));
-        ++pk_issued;
-        if (blk == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // x may come from the previous grid
-        for (int h = 0; h < 2; ++h) {
-          const int i = 2 * blk + h, xs = i % XS;
-          if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(x_full(xs), X_BYTES);
-          tma_load_2d(xs_s + xs * X_BYTES, &tmap_x, i * HK, m0, x_full(xs));
-          ++x_issued;
-        }
-      }
-      // every issued copy must land before the CTA may exit
-      for (int b = pk_issued > PS ? pk_issued - PS : 0; b < pk_issued; ++b)
-        if (!mbar_wait(pk_full(b % PS), (b / PS) & 1)) ok = false;
-      for (int i = x_issued > XS ? x_issued - XS : 0; i < x_issued; ++i)
-        if (!mbar_wait(x_full(i % XS), (i / XS) & 1)) ok = false;
-      if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-      constexpr uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(BMX >> 3) << 17) | ((uint32_t)(BN >> 4) << 24);
-      int gi = 0;                 // groups started so far; buffer gi % 2, its use gi / 2
-      bool fresh = true;          // next MMA starts a group
-      for (int i = 0; i < nhalf && ok; ++i) {
-        const int xs = i % XS, ws = i % WS;
-        if (!mbar_wait(x_full(xs), (i / XS) & 1) || !mbar_wait(w_full(ws), (i / WS) & 1)) { ok = false; break; }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t ad = smem_desc_sw128(ws_s + ws * W_BYTES);     // A: weights, 128 rows
-        const uint64_t bd = smem_desc_sw128(xs_s + xs * X_BYTES);     // B: x, 256 rows
-        for (int cc = 0; cc < 2 && ok; ++cc) {
-          const int c = 2 * i + cc;
-          const int b = gi & 1;
-          if (fresh && gi >= 2 && !mbar_wait(p_empty(b), ((gi >> 1) - 1) & 1)) { ok = false; break; }
-          if (fresh) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t d = tmem + (uint32_t)(b * 256);
-          umma_f16(d, ad + 2 * (2 * cc), bd + 2 * (2 * cc), idesc, fresh ? 0u : 1u);
-          umma_f16(d, ad + 2 * (2 * cc + 1), bd + 2 * (2 * cc + 1), idesc, 1u);
-          fresh = false;
-          if (group_ends(c)) {
-            umma_commit(p_full(b));
-            ++gi;
-            fresh = true;
-          }
-        }
-        umma_commit(x_empty(xs));
-        umma_commit(w_empty(ws));
-      }
-      if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-    }
-  } else if (warp < 2 + kDqWarps) {
-    // ---------------- dequantisers: thread d owns weight rows n0 + d + 64 r, r = 0, 1 ----------------
-    const int d0 = tid - 64;
-    uint32_t zq[2][4];
-    auto load_zeros = [&](int blk, uint32_t (&z)[2][4]) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          z[r][c] = prep_zero_l<T, BITS>(__ldg(&a.z_r[(size_t)cg[blk * 4 + c] * a.Np + n0 + d0 + 64 * r]));
-    };
-    if (nblocks > 0) load_zeros(0, zq);
-    for (int blk = 0; blk < nblocks && ok; ++blk) {
-      const int ps = blk % PS;
-      if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
-      const uint8_t* stage = pk + ps * PKB;
-      uint32_t zn[2][4];
-      if (blk + 1 < nblocks) load_zeros(blk + 1, zn);     // next block's zeros, ahead of use
-      for (int h = 0; h < 2; ++h) {
-        const int i = 2 * blk + h, ws = i % WS;
-        if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int d = d0 + 64 * r;
-          Words<BITS> lw[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) stage_words<BITS>(lw[t], stage, d, t);
-          uint8_t* row = base + S::w + ws * W_BYTES + d * 128;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * h + cc;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              uint4 o;
-              o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[r][c]);
-              o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[r][c]);
-              o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[r][c]);
-              o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[r][c]);
-              const int j = 4 * cc + t;                       // 16-byte chunk (8 k) inside the 64-k row
-              *reinterpret_cast<uint4*>(row + ((j ^ (d & 7)) << 4)) = o;
-            }
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(w_full(ws));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pk_empty(ps));           // both halves of this block are written
-      if (blk + 1 < nblocks) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) zq[r][c] = zn[r][c];
-      }
-    }
-    if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-  } else {
+  if (warp >= kScWarp0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsScaler));
     // ---------------- scalers: S += scale * P per group, then y ----------------
-    const int sw = warp - (2 + kDqWarps);
+    const int sw = warp - kScWarp0;
     const int q = warp & 3;                   // TMEM lane quarter this warp may access
-    const int cs = sw >> 2;                   // 64-column slice of the 256 x rows
+    const int hs = sw >> 2;                   // 128-column half of the 256 x rows
     const int nrow = 32 * q + lane;           // weight row of this thread inside the tile
     const int n = n0 + nrow;
-    float acc[64];
+    float acc[128];
 #pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = 0.f;
+    for (int j = 0; j < 128; ++j) acc[j] = 0.f;
     int gi = 0;
     float sc_next = 0.f;
-    int c_next = 0;
     // the scale of the group that starts at chunk c
     auto scale_at = [&](int c) { return scale_f<T>(__ldg(&a.s_r[(size_t)cg[c] * a.Np + n])); };
     if (nchunks > 0) sc_next = scale_at(0);
     for (int c = 0; c < nchunks && ok; ++c) {
       if (!group_ends(c)) continue;
       const float sc = sc_next;
-      c_next = c + 1;
-      if (c_next < nchunks) sc_next = scale_at(c_next);     // next group's scale, ahead of use
+      if (c + 1 < nchunks) sc_next = scale_at(c + 1);     // next group's scale, ahead of use
       const int b = gi & 1;
       if (!mbar_wait(p_full(b), (gi >> 1) & 1)) { ok = false; break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256 + 64 * cs);
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256 + 128 * hs);
+      uint32_t ra[16], rb[16];
+      tmem_ld16(taddr, ra);
+      tmem_wait_ld(ra);
 #pragma unroll
-      for (int part = 0; part < 8; ++part) {
-        uint32_t r[8];
-        tmem_ld8(taddr + 8 * part, r);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      for (int part = 0; part < 8; part += 2) {
+        tmem_ld16(taddr + 16 * (part + 1), rb);             // next 16 columns in flight while ra is used
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[8 * part + j] = fmaf(sc, __uint_as_float(r[j]), acc[8 * part + j]);
+        for (int j = 0; j < 16; ++j) acc[16 * part + j] = fmaf(sc, __uint_as_float(ra[j]), acc[16 * part + j]);
+        tmem_wait_ld(rb);
+        if (part + 2 < 8) tmem_ld16(taddr + 16 * (part + 2), ra);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[16 * (part + 1) + j] = fmaf(sc, __uint_as_float(rb[j]), acc[16 * (part + 1) + j]);
+        if (part + 2 < 8) tmem_wait_ld(ra);
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
@@ -379,14 +329,149 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       ++gi;
     }
     if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-    // y[m][n] for the 64 x rows of this slice: lanes are consecutive n, so each store is 64 bytes
+    // y[m][n] for the 128 x rows of this half: lanes are consecutive n, so each store is 64 bytes
     uint16_t* y = static_cast<uint16_t*>(a.y);
     if (n < a.N) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int m = m0 + 64 * cs + j;
+      for (int j = 0; j < 128; ++j) {
+        const int m = m0 + 128 * hs + j;
         if (m < a.M) y[(size_t)m * a.N + n] = to_bits<T>(acc[j]);
       }
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsLight));
+    if (warp == 0) {
+      // ---------------- producer ----------------
+      if (lane == 0) {
+        int pk_issued = 0, x_issued = 0;
+        for (int blk = 0; blk < nblocks && ok; ++blk) {
+          const int ps = blk % PS;
+          if (blk >= PS && !mbar_wait(pk_empty(ps), ((blk / PS) - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(pk_full(ps), PKB);
+          const uint8_t* src = a.wr + ((size_t)blk * BITS * a.Np + n0) * 16;
+  #pragma unroll
+          for (int v = 0; v < BITS; ++v)
+            bulk_g2s(smem_u32(pk + ps * PKB + v * BN * 16), src + (size_t)v * a.Np * 16, BN * 16, pk_full(ps));
+          ++pk_issued;
+          if (blk == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // x may come from the previous grid
+          for (int h = 0; h < 2; ++h) {
+            const int i = 2 * blk + h, xs = i % XS;
+            if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
+            mbar_arrive_expect_tx(x_full(xs), X_BYTES);
+            tma_load_2d(xs_s + xs * X_BYTES, &tmap_x, i * HK, m0, x_full(xs));
+            ++x_issued;
+          }
+        }
+        // every issued copy must land before the CTA may exit
+        for (int b = pk_issued > PS ? pk_issued - PS : 0; b < pk_issued; ++b)
+          if (!mbar_wait(pk_full(b % PS), (b / PS) & 1)) ok = false;
+        for (int i = x_issued > XS ? x_issued - XS : 0; i < x_issued; ++i)
+          if (!mbar_wait(x_full(i % XS), (i / XS) & 1)) ok = false;
+        if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      // The whole warp runs the schedule and every lane waits; one elected lane issues the MMAs and
+      // commits as predicated instructions.  Group boundaries come from a register copy of gmask
+      // (loaded one 32-chunk window ahead) and the waits only poison the limit, so nothing between
+      // two MMAs depends on a shared-memory value.  Measured on sm_103a: this keeps tcgen05.mma at
+      // its full rate, where the same loop run by lane 0 alone lost ~40%.
+      {
+        constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+        constexpr uint32_t idesc = (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(BMX >> 3) << 17) | ((uint32_t)(BN >> 4) << 24);
+        const uint32_t me = elect_one();
+        uint64_t limit = kWaitLimitNs;
+        uint32_t cur = gmask[0];
+        uint32_t nxt = nwin > 1 ? gmask[1] : 0u;
+        int gi = 0;                 // groups started so far; buffer gi % 2, its use gi / 2
+        uint32_t fresh = 1;         // next MMA starts a group
+        int xs = 0, ws = 0;
+        uint32_t xph = 0, wph = 0;
+        for (int i = 0; i < nhalf; ++i) {
+          mbar_wait_poison(x_full(xs), xph, limit);
+          mbar_wait_poison(w_full(ws), wph, limit);
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint64_t ad = smem_desc_sw128(ws_s + ws * W_BYTES);     // A: weights, 128 rows
+          const uint64_t bd = smem_desc_sw128(xs_s + xs * X_BYTES);     // B: x, 256 rows
+  #pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * i + cc;
+            if ((c & 31) == 0 && c > 0) {
+              cur = nxt;
+              nxt = (c >> 5) + 1 < nwin ? gmask[(c >> 5) + 1] : 0u;
+            }
+            const int b = gi & 1;
+            if (fresh && gi >= 2) {
+              mbar_wait_poison(p_empty(b), ((gi >> 1) - 1) & 1, limit);
+              asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            }
+            const uint32_t d = tmem + (uint32_t)(b * 256);
+            umma_f16_if(d, ad + 4 * cc, bd + 4 * cc, idesc, fresh ^ 1u, me);
+            umma_f16_if(d, ad + 4 * cc + 2, bd + 4 * cc + 2, idesc, 1u, me);
+            const uint32_t end = (cur >> (c & 31)) & 1u;
+            umma_commit_if(p_full(b), end & me);
+            gi += (int)end;
+            fresh = end;
+          }
+          umma_commit_if(x_empty(xs), me);
+          umma_commit_if(w_empty(ws), me);
+          if (++xs == XS) { xs = 0; xph ^= 1u; }
+          if (++ws == WS) { ws = 0; wph ^= 1u; }
+        }
+        // every MMA must have landed before tensor memory is released
+        umma_commit_if(mma_done, me);
+        mbar_wait_poison(mma_done, 0, limit);
+        if (limit == 0 && me) atomicExch(a.err, DEV_ERR_TIMEOUT);
+      }
+    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+      // ---------------- dequantisers: thread owns weight row n0 + nrow ----------------
+      const int nrow = 32 * (warp - kDqWarp0) + lane;
+      const size_t zcol = (size_t)n0 + nrow;
+      uint32_t zq[4];
+      auto load_zeros = [&](int blk, uint32_t (&z)[4]) {
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) z[c] = prep_zero_l<T, BITS>(__ldg(&a.z_r[(size_t)cg[blk * 4 + c] * a.Np + zcol]));
+      };
+      if (nblocks > 0) load_zeros(0, zq);
+      for (int blk = 0; blk < nblocks && ok; ++blk) {
+        const int ps = blk % PS;
+        if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
+        const uint8_t* stage = pk + ps * PKB;
+        uint32_t zn[4];
+        if (blk + 1 < nblocks) load_zeros(blk + 1, zn);     // next block's zeros, ahead of use
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * blk + h, ws = i % WS;
+          if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
+          Words<BITS> lw[4] = {};
+  #pragma unroll
+          for (int t = 0; t < 4; ++t) half_words<BITS>(lw[t], stage, nrow, t, h);
+          uint8_t* row = base + S::w + ws * W_BYTES + nrow * 128;
+  #pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * h + cc;
+  #pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint4 o;
+              o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[c]);
+              o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[c]);
+              o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[c]);
+              o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[c]);
+              const int j = 4 * cc + t;                         // 16-byte chunk (8 k) inside the 64-k row
+              *reinterpret_cast<uint4*>(row + ((j ^ (nrow & 7)) << 4)) = o;
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(w_full(ws));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pk_empty(ps));           // both halves of this block are written
+        if (blk + 1 < nblocks) {
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) zq[c] = zn[c];
+        }
+      }
+      if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
     }
   }
 
@@ -424,12 +509,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int BITS> size_t large_smem_bytes(int Kr) { return 1024 + LargeSmem<BITS>::cg + (size_t)(Kr / 32) * 4; }
+template <int BITS> size_t large_smem_bytes(int Kr) {
+  return 1024 + LargeSmem<BITS>::cg + (size_t)(Kr / 32) * 4 + (size_t)((Kr / 32 + 31) / 32) * 4;
+}
 
 template <typename T, int BITS>
 cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
   const size_t smem = large_smem_bytes<BITS>(h.Kr);
   auto kern = k_gemm_large<T, BITS>;
+  // setmaxnreg redistributes the registers the block is launched with; a launch with fewer than
+  // kRegsLaunch a thread could never satisfy the scalers' increase, so refuse it.
+  static const int regs = [&] {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G};

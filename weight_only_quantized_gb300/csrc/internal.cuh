@@ -114,6 +114,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (global_ns() - t0 > limit_ns) return false;
   return true;
 }
+// The same bounded wait as one asm block whose only output is the limit: on a timeout it sets
+// limit_ns to 0, so every later wait polls once and falls through.  A thread that issues
+// tcgen05.mma uses this form: when a branch or an operand between two MMAs depends on a value
+// read from shared memory (a wait result, a flag), the MMA issue rate drops by 2.5-4x on sm_103a
+// (measured); a wait whose result feeds only the next wait's limit keeps the full rate.
+__device__ __forceinline__ void mbar_wait_poison(uint32_t bar, uint32_t parity, uint64_t& limit_ns) {
+  asm volatile("{\n\t.reg .pred p;\n\t.reg .u64 t0, t1;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "@p bra WP_END;\n\t"
+               "mov.u64 t0, %%globaltimer;\n\t"
+               "WP_LOOP:\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "@p bra WP_END;\n\t"
+               "mov.u64 t1, %%globaltimer;\n\t"
+               "sub.u64 t1, t1, t0;\n\t"
+               "setp.lt.u64 p, t1, %0;\n\t"
+               "@p bra WP_LOOP;\n\t"
+               "mov.u64 %0, 0;\n\t"
+               "WP_END:\n\t}"
+               : "+l"(limit_ns) : "r"(bar), "r"(parity) : "memory");
+}
 // Bulk copy global -> this CTA's shared memory, completing tx bytes on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
