@@ -95,7 +95,7 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
  *            read back the g_idx check.  The checkpoint buffers may be freed or changed as soon
  *            as the call returns; the handle holds its own copy in its runtime layout.
  *   out      receives the handle (set to NULL on failure).
- * The handle allocates its runtime layout (about K*N*bits/8 bytes plus 3*G*N) and a workspace
+ * The handle allocates its runtime layout (about K*N*bits/8 bytes plus 6*G*N) and a workspace
  * for gptq_gemm calls with M <= 16; gptq_reserve enlarges the workspace.  The handle is
  * immutable: after any change to the weights, build a new one.
  * Errors: INVALID_ARG, UNSUPPORTED, SHAPE, ALIGNMENT, DEVICE, INVALID_GIDX, CUDA.

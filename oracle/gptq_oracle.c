@@ -312,8 +312,11 @@ int oracle_check_rules(int bits, int qw_rows, int qw_cols, int qz_rows, int qz_c
  *    jw = p / F, field f = p % F, bit 16h + bp*f.  The lane's words are numbered
  *    q = t*bp + jw (bp words per lane, 4*bp per (block, column)); vector v = q / 4, word
  *    q % 4 inside the 16-byte vector.  Vectors of plane 0 come first, then plane 1.
- *    Byte offset of the word: ((B*bits + vbase + v) * Np + n) * 16 + 4 * (q % 4), with vbase
- *    the number of vectors of earlier planes (0, or 2 for 3-bit plane 1).
+ *    Byte offset of the word: ((B*bits + V) * Np + pos(V, n)) * 16 + 4 * (q % 4), with
+ *    V = vbase + v, vbase the number of vectors of earlier planes (0, or 2 for 3-bit plane 1),
+ *    and pos(V, n) = 32*(n/32) + (n%32 + rot(V)) % 32: inside each group of 32 columns the
+ *    column order of vector V is rotated by rot(V) = 2V for 4-bit, 2*(V/2) for 8-bit, 4V for
+ *    2-bit and for the 2-bit plane of 3-bit, 0 for the 1-bit plane of 3-bit.
  * 5. S_r[g][n] (n < Np): the scale bits, 0 for pad columns.  Z_r[g][n]: the stored zero
  *    (z - 1) as one byte, 0 for pad columns.
  * Sizes: wr = Kr/128 * bits * Np * 16 bytes; perm Kr int32; cgid Kr/32 int32; S_r, Z_r G*Np.
@@ -331,6 +334,14 @@ int oracle_runtime_dims(const int32_t* g_idx, int K, int N, int group_size, int*
   *Kr_out = (int)((Ks + 127) / 128 * 128);
   *Np_out = (N + 255) / 256 * 256;
   return ORACLE_OK;
+}
+
+/* Column rotation of vector V inside a group of 32 columns (step 4 above). */
+static long column_rotation(int bits, long V) {
+  if (bits == 4) return 2 * V;
+  if (bits == 8) return 2 * (V / 2);
+  if (bits == 2) return 4 * V;
+  return V < 2 ? 4 * V : 0;   /* 3-bit: 2-bit plane vectors 0, 1; 1-bit plane vector 2 */
 }
 
 int oracle_runtime_layout(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
@@ -366,7 +377,9 @@ int oracle_runtime_layout(const int32_t* qweight, const int32_t* qzeros, const u
         uint32_t val = bits == 3 ? (pl == 0 ? (code & 3u) : (code >> 2)) : code;
         long F = 16 / bp, jw = p / F, f = p % F;
         long q = t * bp + jw, v = q / 4;
-        size_t off = ((size_t)(B * bits + vbase + v) * Np + n) * 16 + 4 * (q % 4);
+        long V = vbase + v;
+        long pos = n / 32 * 32 + (n % 32 + column_rotation(bits, V)) % 32;
+        size_t off = ((size_t)(B * bits + V) * Np + pos) * 16 + 4 * (q % 4);
         uint32_t* word = (uint32_t*)(wr + off);
         *word |= val << (16 * h + bp * f);
         vbase += bp;

@@ -32,7 +32,12 @@ def _decode_layout(L, bits, N):
         jw, f = p // F, p % F
         q = t * bp + jw
         v = q // 4
-        word_idx = ((B * bits + vbase + v)[:, None] * Np + np.arange(N)[None, :]) * 4 + (q % 4)[:, None]
+        V = vbase + v
+        n = np.arange(N)[None, :]
+        # inside a group of 32 columns, vector V's columns are rotated by rot(V)
+        rot = {4: 2 * V, 8: 2 * (V // 2), 2: 4 * V, 3: np.where(V < 2, 4 * V, 0)}[bits][:, None]
+        pos = n // 32 * 32 + (n % 32 + rot) % 32
+        word_idx = ((B * bits + V)[:, None] * Np + pos) * 4 + (q % 4)[:, None]
         val = (words[word_idx].astype(np.int64) >> (16 * h + bp * f)[:, None]) & ((1 << bp) - 1)
         codes |= val << shift_into_code
     return codes

@@ -40,6 +40,7 @@ static void free_handle(Handle* h) {
   cudaFree(h->cgid);
   cudaFree(h->s_r);
   cudaFree(h->z_r);
+  cudaFree(h->zst);
   cudaFree(h->xp);
   cudaFree(h->err);
   delete h;
@@ -259,7 +260,7 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->reserved_M = h.reserved_M;
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
-                       (size_t)h.G * h.Np * 3 + h.xp_bytes;
+                       (size_t)h.G * h.Np * 6 + h.xp_bytes;
   return GPTQ_OK;
 }
 

@@ -97,44 +97,27 @@ template <typename T> __device__ __forceinline__ float scale_f(uint16_t b);
 template <> __device__ __forceinline__ float scale_f<__half>(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 template <> __device__ __forceinline__ float scale_f<__nv_bfloat16>(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
-// Words of one lane (t = 0..3) of one column from a packed stage laid out [vector][column][16 B].
+// Words of one lane (t = 0..3) of one column.
 template <int BITS> struct Words { uint32_t w[BITS]; };
-template <int BITS>
-__device__ __forceinline__ void stage_words(Words<BITS>& o, const uint8_t* stage, int d, int t) {
-  if constexpr (BITS == 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(stage + ((size_t)t * BN + d) * 16);
-    o.w[0] = v.x; o.w[1] = v.y; o.w[2] = v.z; o.w[3] = v.w;
-  } else if constexpr (BITS == 2) {
-    const uint2 v = *reinterpret_cast<const uint2*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1));
-    o.w[0] = v.x; o.w[1] = v.y;
-  } else if constexpr (BITS == 8) {
-    const uint4 v0 = *reinterpret_cast<const uint4*>(stage + ((size_t)(2 * t) * BN + d) * 16);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(stage + ((size_t)(2 * t + 1) * BN + d) * 16);
-    o.w[0] = v0.x; o.w[1] = v0.y; o.w[2] = v0.z; o.w[3] = v0.w;
-    o.w[4] = v1.x; o.w[5] = v1.y; o.w[6] = v1.z; o.w[7] = v1.w;
-  } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1));
-    o.w[0] = v.x; o.w[1] = v.y;
-    o.w[2] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)2 * BN + d) * 16 + 4 * t);
-  }
-}
 
 // The words of lane t that chunks 2h and 2h + 1 of a 128-row block use (other entries untouched):
 // 4-bit: word c of vector t; 2-bit: word c/2; 8-bit: words 2c, 2c+1 (vector 2t + h); 3-bit: word
 // c/2 of the 2-bit plane and the lane's word of the 1-bit plane.
 template <int BITS>
 __device__ __forceinline__ void half_words(Words<BITS>& o, const uint8_t* stage, int d, int t, int h) {
+  // a stage holds, per vector, the 128 columns of the tile: column d of vector v at code_col_pos
+  auto at = [&](int v) { return stage + ((size_t)v * BN + code_col_pos(BITS, v, d)) * 16; };
   if constexpr (BITS == 4) {
-    const uint2 v = *reinterpret_cast<const uint2*>(stage + ((size_t)t * BN + d) * 16 + 8 * h);
+    const uint2 v = *reinterpret_cast<const uint2*>(at(t) + 8 * h);
     o.w[2 * h] = v.x; o.w[2 * h + 1] = v.y;
   } else if constexpr (BITS == 2) {
-    o.w[h] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1) + 4 * h);
+    o.w[h] = *reinterpret_cast<const uint32_t*>(at(t >> 1) + 8 * (t & 1) + 4 * h);
   } else if constexpr (BITS == 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(stage + ((size_t)(2 * t + h) * BN + d) * 16);
+    const uint4 v = *reinterpret_cast<const uint4*>(at(2 * t + h));
     o.w[4 * h] = v.x; o.w[4 * h + 1] = v.y; o.w[4 * h + 2] = v.z; o.w[4 * h + 3] = v.w;
   } else {
-    o.w[h] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)(t >> 1) * BN + d) * 16 + 8 * (t & 1) + 4 * h);
-    o.w[2] = *reinterpret_cast<const uint32_t*>(stage + ((size_t)2 * BN + d) * 16 + 4 * t);
+    o.w[h] = *reinterpret_cast<const uint32_t*>(at(t >> 1) + 8 * (t & 1) + 4 * h);
+    o.w[2] = *reinterpret_cast<const uint32_t*>(at(2) + 4 * t);
   }
 }
 
@@ -493,22 +476,6 @@ __global__ void k_permute_x(const uint16_t* __restrict__ x, const int32_t* __res
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
 template <int BITS> size_t large_smem_bytes(int Kr) {
   return 1024 + LargeSmem<BITS>::cg + (size_t)(Kr / 32) * 4 + (size_t)((Kr / 32 + 31) / 32) * 4;
 }
@@ -551,6 +518,18 @@ cudaError_t launch_t(const Handle& h, const CUtensorMap& map, void* y, int M, cu
 }
 
 }  // namespace
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
 
 bool large_m_available() { return true; }
 

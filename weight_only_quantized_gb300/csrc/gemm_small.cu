@@ -1,49 +1,67 @@
-// Small-M GEMM (decode, M <= 16): weight streaming at HBM speed.
+// Small-M GEMM (decode, M <= 16): a persistent weight stream at HBM speed.
 //
 // mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin, Machete": at small M "only the
 // weight bytes matter" (opening section); the quantised weight only pays if it stays packed
 // until the registers that feed the tensor core; a group scale cannot be hoisted out of the k
-// reduction (section on the LOP3 dequant and the scale); for tiny M the lever is many CTAs
-// streaming weights at once, and the skinny operand goes in the MMA's N slot (swap-AB, section
+// reduction (section on the LOP3 dequant and the scale); for tiny M the lever is every SM
+// streaming weights at once, with the skinny operand in the MMA's N slot (swap-AB, section
 // "Where the batch-size crossover is" and the M-bucketed dispatch discussion).
 //
-// Design on sm_103a (each point measured on GB300):
-//  * Programmatic dependent launch.  A CTA first lets the next grid on the stream launch, starts
-//    its weight stream (weights belong to the handle and never depend on earlier work), and only
-//    then waits (griddepcontrol.wait) for the previous grid before it reads x or writes y.  Back to
-//    back, a 29 MB read kernel drops from 8.2 us to 4.2 us this way.
-//  * A CTA owns NCW x 32 output features and, normally, all of K: its eight warps are NCW column
-//    warps times 8/NCW k-groups, each k-group a contiguous slice of the 128-row blocks.  Partial
-//    sums of the k-groups meet once in shared memory at the end.  Only when x for the whole K
-//    would not fit in shared memory is K split across the CTAs of a thread-block cluster, reduced
-//    through distributed shared memory in fixed rank order.  No workspace, no atomics.
-//  * Every lane streams its own lane words with cp.async into a private slot of its warp's
-//    shared-memory ring (STAGES blocks deep): no registers held by loads in flight, no barriers.
+// Design on sm_103a:
+//  * One CTA per SM, each owning a balanced run of 32-column tiles.  For every tile it streams
+//    the 128-row blocks of packed codes with one 2-D TMA box per block (its bits vectors of 512
+//    bytes; 512-byte bulk copies were issue-bound) into a ring of stages several tens of KB deep, so each SM keeps enough bytes
+//    in flight to saturate its share of HBM from the first microsecond.  One producer warp issues
+//    the copies; eight consumer warps take the blocks of a tile round robin.
+//  * Programmatic dependent launch: the producer starts the weight stream (handle-owned data),
+//    and only then waits (griddepcontrol.wait) for the previous grid before it copies x; the
+//    consumers write y only after x has arrived.  The CTA needs at most half an SM's shared
+//    memory, so the next call's CTAs start streaming while this call finishes.
+//  * x is staged per K-panel (all of K when it fits) by bulk copies into rows 64 bytes apart
+//    modulo 128, so a lane's 8-byte fragment load meets at most one other lane on its banks.
+//    With act-order, a small gather kernel first writes x in sorted k order into the handle's
+//    workspace.
+//  * Zeros and scales come from a tile-major copy of the runtime layout (per tile and group 32
+//    zero bytes and 32 scales, permuted so that the four columns of a lane are adjacent): one
+//    bulk copy per tile and panel, then two shared loads per lane per 32-row chunk.
 //  * mma.sync.m16n8k16 with swap-AB: A = weights (16 output features x 16 k), B = x^T (16 k x 8
-//    batch rows), fp32 accumulators.
+//    batch rows), fp32 accumulators; each chunk's partial sum is scaled into the total in fp32.
 //  * Conversion: one LOP3 puts two codes into the mantissas of a magic fp16 (1024) or bf16 (128)
 //    pair (exactly magic + code), one packed subtract of (magic + zero) leaves the exact integer
-//    code - zero; the LOP3 (and the shift for fields above the low one) runs on the integer pipe,
-//    the subtract on the fp16 pipe.  8-bit codes with bf16 go through the 2^23 fp32 magic because
-//    bf16 holds 128 + q exactly only for q < 128.  The group scale multiplies each group's fp32
-//    partial sum; the runtime layout keeps every MMA step inside one 32-row chunk, hence inside one
-//    group.
+//    code - zero.  8-bit codes with bf16 go through the 2^23 fp32 magic because bf16 holds
+//    128 + q exactly only for q < 128.
+//  * Every wait is bounded; a timeout sets the handle's error word, and the CTA drains its copies
+//    and exits.
 #include "internal.cuh"
 
 #include <algorithm>
+#include <cstring>
 #include <type_traits>
 
 namespace gptq {
 namespace {
 
-constexpr int kMaxSplit = 8;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kXsBudget = 48 * 1024;       // shared memory for staged x before K is split over a cluster
+constexpr int kCW = 8;                       // consumer warps
+constexpr int kThreadsS = (kCW + 1) * 32;    // + one producer warp
+constexpr int kTileN = 32;                   // output features per tile
+constexpr int kZsRow = 96;                   // bytes of one (tile, group) row of zst
+constexpr int kSmemHalf = 110 * 1024;        // two CTAs (consecutive calls) share an SM
+constexpr int kSmemFull = 227 * 1024;
+constexpr int kXSmall = 24 * 1024;           // x for all of K up to this size: half an SM
+constexpr int kXSingle = 136 * 1024;         // up to this size: x staged once, a whole SM
+constexpr int kXPanel = 64 * 1024;           // otherwise per K-panel of this size, double buffered
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <typename T> struct Magic;
 template <> struct Magic<__half> { static constexpr uint32_t bits = 0x6400u; };
 template <> struct Magic<__nv_bfloat16> { static constexpr uint32_t bits = 0x4300u; };
+
+// One stage = kSmallBlocksPerBox 128-row blocks of one 32-column tile, copied densely by a single
+// TMA box: block u's vector v (32 columns) at (u * BITS + v) * 512, column order rotated per
+// vector by the runtime layout so that the consumers' reads are free of bank conflicts.  Boxes of
+// one block (2 KB at 4 bits) left the stream limited by copies in flight; four blocks are 8 KB.
+constexpr int kSPB = kSmallBlocksPerBox;
+template <int BITS> __host__ __device__ constexpr int stage_bytes() { return kSPB * BITS * 512; }
 
 template <typename T>
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1);
@@ -88,6 +106,13 @@ template <typename T> __device__ __forceinline__ float to_float(uint32_t b);
 template <> __device__ __forceinline__ float to_float<__half>(uint32_t b) { return __half2float(__ushort_as_half((uint16_t)b)); }
 template <> __device__ __forceinline__ float to_float<__nv_bfloat16>(uint32_t b) { return __uint_as_float(b << 16); }
 
+// 1 in exactly one lane of the (converged) warp.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+  return pred;
+}
+
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -98,7 +123,7 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // 8-bit codes with bf16 activations go through fp32; every other case uses the fp16/bf16 magic.
 template <typename T, int BITS> constexpr bool kViaF32 = BITS == 8 && std::is_same<T, __nv_bfloat16>::value;
 
-// Zero point (stored + 1) in the form code_minus_zero subtracts.
+// Zero point (stored + 1) in the form operand() subtracts.
 template <typename T, int BITS>
 __device__ __forceinline__ uint32_t prep_zero(uint32_t stored) {
   const uint32_t z = stored + 1u;
@@ -131,214 +156,203 @@ __device__ __forceinline__ uint32_t operand(const LaneWords<BITS>& lw, int p, ui
   }
 }
 
-// ---- per-lane cp.async ring ----
-// A slot holds one block for one warp: [row idx 0..3][lane][bytes of that row], plane after plane
-// for bits 3, so every lane reads and writes 16-, 8- or 4-byte words at a 16-, 8- or 4-byte stride.
-template <int BITS> __host__ __device__ constexpr int slot_bytes() { return 4 * 32 * BITS * 4; }
-template <int BITS> __host__ __device__ constexpr int ring_stages() { return BITS == 8 ? 2 : BITS == 2 ? 6 : 3; }
-
-template <int N>
-__device__ __forceinline__ void cp_async(uint32_t dst, const void* src) {
-  if constexpr (N == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" :: "r"(dst), "l"(src), "n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-
-// Issue this lane's copies of block B, rows n[idx] (idx = 2 * tile + r), into slot base `dst`.
+// Byte offsets, inside one block of a stage, of this lane's words: vector v of column c sits at
+// v * 512 + 16 * code_col_pos(c).  Lane (g, t) owns columns g + 8 idx, idx = 0..3, and lane t's
+// words (4-bit: vector t; 8-bit: vectors 2t, 2t+1; 2-bit: half t%2 of vector t/2; 3-bit: that,
+// plus word t of the 1-bit-plane vector 2).  Lane constants, computed once.
+template <int BITS> struct LaneOffsets { int o[4]; int o2[4]; };
 template <int BITS>
-__device__ __forceinline__ void issue_block(uint32_t dst, const uint8_t* __restrict__ wr, long B, int Np,
-                                            const int (&n)[4], int t, int lane) {
+__device__ __forceinline__ LaneOffsets<BITS> lane_offsets(int g, int t) {
+  LaneOffsets<BITS> L;
+  auto at = [&](int v, int c) { return v * 512 + code_col_pos(BITS, v, c) * 16; };
 #pragma unroll
   for (int idx = 0; idx < 4; ++idx) {
-    if constexpr (BITS == 4) {
-      cp_async<16>(dst + (idx * 32 + lane) * 16, wr + (((size_t)B * 4 + t) * Np + n[idx]) * 16);
-    } else if constexpr (BITS == 2) {
-      cp_async<8>(dst + (idx * 32 + lane) * 8, wr + (((size_t)B * 2 + (t >> 1)) * Np + n[idx]) * 16 + 8 * (t & 1));
-    } else if constexpr (BITS == 8) {
-      cp_async<16>(dst + ((2 * idx) * 32 + lane) * 16, wr + (((size_t)B * 8 + 2 * t) * Np + n[idx]) * 16);
-      cp_async<16>(dst + ((2 * idx + 1) * 32 + lane) * 16, wr + (((size_t)B * 8 + 2 * t + 1) * Np + n[idx]) * 16);
-    } else {
-      cp_async<8>(dst + (idx * 32 + lane) * 8, wr + (((size_t)B * 3 + (t >> 1)) * Np + n[idx]) * 16 + 8 * (t & 1));
-      cp_async<4>(dst + 1024 + (idx * 32 + lane) * 4, wr + (((size_t)B * 3 + 2) * Np + n[idx]) * 16 + 4 * t);
-    }
+    const int c = g + 8 * idx;
+    if constexpr (BITS == 4) { L.o[idx] = at(t, c); L.o2[idx] = 0; }
+    else if constexpr (BITS == 8) { L.o[idx] = at(2 * t, c); L.o2[idx] = at(2 * t + 1, c); }
+    else if constexpr (BITS == 2) { L.o[idx] = at(t >> 1, c) + 8 * (t & 1); L.o2[idx] = 0; }
+    else { L.o[idx] = at(t >> 1, c) + 8 * (t & 1); L.o2[idx] = at(2, c) + 4 * t; }
   }
+  return L;
 }
-
 template <int BITS>
-__device__ __forceinline__ void read_block(LaneWords<BITS> (&lw)[4], const uint8_t* slot, int lane) {
+__device__ __forceinline__ void read_block(LaneWords<BITS> (&lw)[4], const uint8_t* blk, const LaneOffsets<BITS>& L) {
 #pragma unroll
   for (int idx = 0; idx < 4; ++idx) {
     if constexpr (BITS == 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(slot + (idx * 32 + lane) * 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(blk + L.o[idx]);
       lw[idx].w[0] = v.x; lw[idx].w[1] = v.y; lw[idx].w[2] = v.z; lw[idx].w[3] = v.w;
     } else if constexpr (BITS == 2) {
-      const uint2 v = *reinterpret_cast<const uint2*>(slot + (idx * 32 + lane) * 8);
+      const uint2 v = *reinterpret_cast<const uint2*>(blk + L.o[idx]);
       lw[idx].w[0] = v.x; lw[idx].w[1] = v.y;
     } else if constexpr (BITS == 8) {
-      const uint4 v0 = *reinterpret_cast<const uint4*>(slot + ((2 * idx) * 32 + lane) * 16);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(slot + ((2 * idx + 1) * 32 + lane) * 16);
+      const uint4 v0 = *reinterpret_cast<const uint4*>(blk + L.o[idx]);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(blk + L.o2[idx]);
       lw[idx].w[0] = v0.x; lw[idx].w[1] = v0.y; lw[idx].w[2] = v0.z; lw[idx].w[3] = v0.w;
       lw[idx].w[4] = v1.x; lw[idx].w[5] = v1.y; lw[idx].w[6] = v1.z; lw[idx].w[7] = v1.w;
     } else {
-      const uint2 v = *reinterpret_cast<const uint2*>(slot + (idx * 32 + lane) * 8);
+      const uint2 v = *reinterpret_cast<const uint2*>(blk + L.o[idx]);
       lw[idx].w[0] = v.x; lw[idx].w[1] = v.y;
-      lw[idx].w[2] = *reinterpret_cast<const uint32_t*>(slot + 1024 + (idx * 32 + lane) * 4);
+      lw[idx].w[2] = *reinterpret_cast<const uint32_t*>(blk + L.o2[idx]);
     }
   }
 }
 
-// Parameters of one launch.
+// One 2-D TMA box (global -> this CTA's shared memory), completing its bytes on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+               :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+
+// Launch parameters (one plan per handle and M, cached on the host).
 struct SmallArgs {
-  const uint8_t* wr; const int32_t* perm; const int32_t* cgid; const uint16_t* s_r; const uint8_t* z_r;
-  const void* x; void* y; int32_t* err;
-  int M, N, Np, K, Kr, G, identity, bps, splits, span_max;
-  int g_first[kMaxSplit];    // first group of each split's k-range
+  const uint8_t* wr; const int32_t* cgid; const uint8_t* zst;
+  const uint16_t* x; void* y; int32_t* err;
+  int ldx;          // row stride of x (elements): K for the caller's x, Kr for the gathered copy
+  int M, N, Np, Kr, G;
+  int ntiles;       // 32-column tiles holding at least one column < N
+  int pb;           // 128-row blocks per K-panel
+  int npanel;
+  int single;       // 1: one panel covers K, x is staged once per CTA
+  int lg_rd;        // log2 of the stages in the weight ring (a power of two: slot and phase by mask and shift)
+  int span_max;     // rows of a zero/scale table (groups of one panel)
+  int x_row;        // bytes of one staged x row: pb * 256 + 64 (rows 64 bytes apart mod 128)
+  int o_x, o_zs, o_red, o_cg, o_bar;   // shared-memory offsets; the ring starts at 0
 };
 
-__host__ __device__ inline int round16(int b) { return (b + 15) / 16 * 16; }
-
-// Shared-memory carve-up of one CTA (byte offsets), shared by the kernel and the planner.
-struct SmallSmem { int ring, xs, zs, cg, bgrp, red, total; };
-__host__ __device__ inline SmallSmem small_smem(int slot_b, int stages, int bps, int mrows, int span_max,
-                                               int ncol, int kg, int mt8) {
-  SmallSmem o;
-  o.ring = 0;
-  o.xs = o.ring + kWarps * stages * slot_b;
-  o.zs = o.xs + bps * 8 * mrows * 4 * 8;
-  o.cg = o.zs + span_max * ncol * 8;
-  o.bgrp = o.cg + round16(4 * bps * 4);
-  o.red = o.bgrp + round16(bps * 4);
-  o.total = o.red + kg * mt8 * 8 * (ncol + 4) * 4;
-  return o;
+__device__ __forceinline__ void named_sync_consumers() {
+  asm volatile("bar.sync 1, %0;" :: "n"(kCW * 32) : "memory");
 }
 
-template <typename T, int BITS, int MT8, int NCW>
-__global__ void __launch_bounds__(kThreads) k_gemm_small(const SmallArgs a) {
-  constexpr int KG = kWarps / NCW;
-  constexpr int NCOL = NCW * 32;
-  constexpr int STAGES = ring_stages<BITS>();
-  constexpr int SLOT = slot_bytes<BITS>();
-  constexpr int RS = NCOL + 4;
-  extern __shared__ __align__(128) uint8_t smem[];
+template <typename T, int BITS, int MT8>
+__global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
+  constexpr int SB = stage_bytes<BITS>();
+  constexpr int RS = kTileN + 4;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // TMA boxes land on 128-byte boundaries
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int cw = warp % NCW, kg = warp / NCW;
-  const int n_cta = blockIdx.x * NCOL;
-  const int m0 = blockIdx.z * (MT8 * 8);
-  const int Mr = min(a.M - m0, MT8 * 8);          // x rows this CTA stages and stores
   const int NB = a.Kr / 128;
-  const int blk0 = blockIdx.y * a.bps;
-  const int nblk = max(0, min(NB, blk0 + a.bps) - blk0);
-  const int bpw = (nblk + KG - 1) / KG;            // blocks per k-group
-  const int jb0 = kg * bpw;                        // this warp's first CTA-local block
-  const int nmine = max(0, min(nblk, jb0 + bpw) - jb0);
-  const int g_first = a.g_first[blockIdx.y];
+  const int T0 = (int)(((long)blockIdx.x * a.ntiles) / gridDim.x);
+  const int T1 = (int)(((long)(blockIdx.x + 1) * a.ntiles) / gridDim.x);
+  const int lg = a.lg_rd, rd = 1 << lg;
 
-  const SmallSmem L = small_smem(SLOT, STAGES, a.bps, Mr, a.span_max, NCOL, KG, MT8);
-  uint8_t* ring = smem + L.ring + (size_t)warp * STAGES * SLOT;
-  const uint32_t ring_s = smem_u32(ring);
-  uint2* xs = reinterpret_cast<uint2*>(smem + L.xs);        // [bl][s][m < Mr][t]: 4 sorted k of x row m
-  uint2* zsm = reinterpret_cast<uint2*>(smem + L.zs);       // [span_max][NCOL] (prepared zero, scale bits)
-  int32_t* cg = reinterpret_cast<int32_t*>(smem + L.cg);    // [4*bps] group of each chunk
-  int32_t* bgrp = reinterpret_cast<int32_t*>(smem + L.bgrp);  // [bps] group of a block, -1 if it has several
-  float* red = reinterpret_cast<float*>(smem + L.red);      // [KG][MT8*8][RS]
+  uint8_t* ring = smem;
+  uint8_t* xreg = smem + a.o_x;
+  uint8_t* zsreg = smem + a.o_zs;
+  float* red = reinterpret_cast<float*>(smem + a.o_red);
+  int32_t* cg = reinterpret_cast<int32_t*>(smem + a.o_cg);
+  const uint32_t bar0 = smem_u32(smem + a.o_bar);
+  auto full = [&](int i) { return bar0 + 8u * i; };
+  auto empty = [&](int i) { return bar0 + 8u * (rd + i); };
+  auto hfull = [&](int i) { return bar0 + 8u * (2 * rd + i); };
+  auto hempty = [&](int i) { return bar0 + 8u * (2 * rd + 2 + i); };
+  const int zs_bytes = a.span_max * kZsRow;
+  const int x_bytes = a.M * a.x_row;
 
-  // Let the next grid on the stream launch now; it waits for this one before touching our outputs.
+  // Let the next grid on the stream launch; it waits for this one before touching our outputs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // Rows of this lane: tile i (16 output features), r = 0/1 -> + 8; idx = 2 i + r.
-  int nrow[4];
-#pragma unroll
-  for (int idx = 0; idx < 4; ++idx) nrow[idx] = n_cta + cw * 32 + 16 * (idx >> 1) + 8 * (idx & 1) + g;
-
-  // Start the weight stream (handle-owned data: no dependency on the previous grid).
-#pragma unroll
-  for (int j = 0; j < STAGES - 1; ++j) {
-    if (j < nmine) issue_block<BITS>(ring_s + j * SLOT, a.wr, blk0 + jb0 + j, a.Np, nrow, t, lane);
-    cp_async_commit();
+  if (tid == 0) {
+    for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(hfull(i), 1); mbar_init(hempty(i), kCW); }
+    fence_mbar_init();
   }
+  for (int i = tid; i < NB * 4; i += kThreadsS) cg[i] = __ldg(&a.cgid[i]);
+  __syncthreads();
 
-  // Handle-owned tables.
-  for (int i = tid; i < 4 * nblk; i += kThreads) cg[i] = __ldg(&a.cgid[4 * blk0 + i]);
-  for (int i = tid; i < a.span_max * NCOL; i += kThreads) {
-    const int gg = g_first + i / NCOL;
-    uint2 v = make_uint2(0u, 0u);
-    if (gg < a.G) {
-      const size_t o = (size_t)gg * a.Np + n_cta + (i % NCOL);
-      v = make_uint2(prep_zero<T, BITS>(__ldg(&a.z_r[o])), __ldg(&a.s_r[o]));
-    }
-    zsm[i] = v;
-  }
+  // Blocks of panel p, and the first group a panel touches (cgid ascends in the sorted order).
+  auto panel_blocks = [&](int p) { return min(NB, (p + 1) * a.pb) - p * a.pb; };
 
-  // x may be the previous grid's output.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
-    const uint16_t* x = static_cast<const uint16_t*>(a.x);
-    const int nq = nblk * 32 * Mr;
-    for (int i0 = tid; i0 < nq; i0 += 4 * kThreads) {
-      uint2 v[4];
-      int dst[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kThreads;
-        dst[u] = -1;
-        if (i < nq) {
-          const int m = i % Mr, q = (i / Mr) & 31, bl = i / (Mr * 32);
-          const int j = 128 * (blk0 + bl) + 4 * q;
-          const uint16_t* xr = static_cast<const uint16_t*>(x) + (size_t)(m0 + m) * a.K;
-          if (a.identity) {
-            v[u] = *reinterpret_cast<const uint2*>(xr + j);
-          } else {
-            const int4 kk = __ldg(reinterpret_cast<const int4*>(a.perm + j));
-            const uint32_t e0 = kk.x >= 0 ? xr[kk.x] : 0u, e1 = kk.y >= 0 ? xr[kk.y] : 0u;
-            const uint32_t e2 = kk.z >= 0 ? xr[kk.z] : 0u, e3 = kk.w >= 0 ? xr[kk.w] : 0u;
-            v[u] = make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
-          }
-          const int s = 2 * (q >> 3) + (q & 1), tt = (q & 7) >> 1;
-          dst[u] = ((bl * 8 + s) * Mr + m) * 4 + tt;
+  if (warp == kCW) {
+    // ---------------- producer ----------------
+    // The whole warp runs the schedule and waits; one elected lane issues.  Nothing between two
+    // copies branches on a shared-memory value: the waits only poison the limit (an early-exit
+    // branch on a wait result made each issue wait for the previous copy, ~4x slower here).
+    uint32_t go = elect_one();
+    uint64_t limit = kWaitNs;
+    bool waited = false;            // griddepcontrol.wait done (x may be the previous grid's output)
+    int s_issued = 0;               // weight stages issued
+    int q = 0;                      // segments (tile, panel) started
+    int s_sent = 0, q_sent = 0;     // stages and segment headers actually issued
+    for (int ti = T0; ti < T1; ++ti) {
+      for (int p = 0; p < a.npanel; ++p, ++q) {
+        const int nb = panel_blocks(p);
+        const int hs = q & 1;
+        if (q >= 2) mbar_wait_poison(hempty(hs), ((q >> 1) - 1) & 1, limit);
+        go &= limit != 0 ? 1u : 0u;   // after a timeout nothing more is issued
+        const int gf = cg[4 * p * a.pb], gl = cg[4 * (p * a.pb + nb) - 1];
+        const bool load_x = !a.single || q == 0;
+        const uint32_t zs_tx = (uint32_t)(gl - gf + 1) * kZsRow;
+        const uint32_t x_tx = load_x ? (uint32_t)a.M * nb * 256u : 0u;
+        if (go) {
+          mbar_arrive_expect_tx(hfull(hs), zs_tx + x_tx);
+          bulk_g2s(smem_u32(zsreg + hs * zs_bytes), a.zst + ((size_t)ti * a.G + gf) * kZsRow, zs_tx, hfull(hs));
         }
+        q_sent += go ? 1 : 0;
+        // weights of the first segment (up to 4 stages) go out before x; x waits for the previous grid
+        const int nst = (nb + kSPB - 1) / kSPB;
+        int j = 0;
+        auto issue_stage = [&](int l) {
+          const int s = s_issued;
+          const int slot = s & (rd - 1);
+          if (s >= rd) mbar_wait_poison(empty(slot), (uint32_t)(((s >> lg) - 1) & 1), limit);
+          go &= limit != 0 ? 1u : 0u;
+          if (go) {
+            mbar_arrive_expect_tx(full(slot), (uint32_t)SB);
+            // box: the kSPB * BITS vector rows from block p * pb + kSPB * l on, tile ti's 512 bytes
+            // (64 uint64) of each; rows past the last block read as zero
+            tma_load_2d(smem_u32(ring + (size_t)slot * SB), &wmap, ti * 64, (p * a.pb + kSPB * l) * BITS, full(slot));
+          }
+          s_sent += go ? 1 : 0;
+          ++s_issued;
+        };
+        if (load_x) {
+          const int pre = waited ? 0 : min(nst, min(rd, 4));
+          for (; j < pre; ++j) issue_stage(j);
+          if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
+          if (go) {
+            uint8_t* xd = xreg + (a.single ? 0 : hs * x_bytes);
+            for (int m = 0; m < a.M; ++m)
+              bulk_g2s(smem_u32(xd + m * a.x_row), a.x + (size_t)m * a.ldx + (size_t)p * a.pb * 128,
+                       (uint32_t)nb * 256u, hfull(hs));
+          }
+        }
+        for (; j < nst; ++j) issue_stage(j);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (dst[u] >= 0) xs[dst[u]] = v[u];
     }
+    // every copy issued must land before the CTA may exit.  Issue stops at the first timeout, so
+    // the issued stages are the first s_sent (headers: q_sent), none overwriting an unconsumed
+    // slot; the drain gets a fresh limit since the copies are reads of valid addresses.
+    uint64_t drain = kWaitNs;
+    const int first = s_sent > rd ? s_sent - rd : 0;
+    for (int s = first; s < s_sent; ++s) mbar_wait_poison(full(s & (rd - 1)), (uint32_t)((s >> lg) & 1), drain);
+    for (int qq = q_sent > 2 ? q_sent - 2 : 0; qq < q_sent; ++qq)
+      mbar_wait_poison(hfull(qq & 1), (uint32_t)((qq >> 1) & 1), drain);
+    if ((limit == 0 || drain == 0) && lane == 0) atomicExch(a.err, DEV_ERR_TIMEOUT);
+    return;
   }
-  __syncthreads();
-  for (int bl = tid; bl < nblk; bl += kThreads) bgrp[bl] = cg[4 * bl] == cg[4 * bl + 3] ? cg[4 * bl] : -1;
-  __syncthreads();
 
-  // ---------------- main loop ----------------
+  // ---------------- consumers ----------------
+  // Stages are dealt round robin over the eight warps across segments (stage s to warp s % 8).
+  // Each warp keeps the current group's prepared zeros and scales and its partial sums, and folds
+  // the partial sums into the total (times the scale) only when the group changes.
+  const int g = lane >> 2, t = lane & 3;
+  const LaneOffsets<BITS> LO = lane_offsets<BITS>(g, t);
+  bool ok = true;
+  bool waited = false;
   float acc[2][MT8][4], part[2][MT8][4];
+  bool mval[MT8];
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int mt = 0; mt < MT8; ++mt) mval[mt] = 8 * mt + g < a.M;
+  // this lane's x fragments: row 8 mt + g (row 0 when that row is absent), k offset 8 t inside
+  // each 32-row chunk (the runtime layout's k order: lane t of 16-k step ks holds sorted rows
+  // 4q .. 4q + 3, q = 8 (ks / 2) + 2 t + ks % 2)
+  int xoff[MT8];
 #pragma unroll
-    for (int mt = 0; mt < MT8; ++mt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) { acc[i][mt][q] = 0.f; part[i][mt][q] = 0.f; }
+  for (int mt = 0; mt < MT8; ++mt) xoff[mt] = (mval[mt] ? 8 * mt + g : 0) * a.x_row + 16 * t;
   uint32_t zq[4];
   float sc[4];
-  int cur = -1;
-  const int col0 = cw * 32 + g;          // CTA-local column of idx 0; idx adds 16 (idx >> 1) + 8 (idx & 1)
-  auto load_group = [&](int gg) {
-    const int li = gg - g_first;
-#pragma unroll
-    for (int idx = 0; idx < 4; ++idx) {
-      const int c = col0 + 16 * (idx >> 1) + 8 * (idx & 1);
-      uint2 v;
-      if (li < a.span_max) {
-        v = zsm[li * NCOL + c];
-      } else {
-        const size_t o = (size_t)gg * a.Np + n_cta + c;
-        v = make_uint2(prep_zero<T, BITS>(__ldg(&a.z_r[o])), __ldg(&a.s_r[o]));
-      }
-      zq[idx] = v.x;
-      sc[idx] = to_float<T>(v.y);
-    }
-  };
   auto flush = [&]() {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -349,247 +363,242 @@ __global__ void __launch_bounds__(kThreads) k_gemm_small(const SmallArgs a) {
         acc[i][mt][2] = fmaf(sc[2 * i + 1], part[i][mt][2], acc[i][mt][2]);
         acc[i][mt][3] = fmaf(sc[2 * i + 1], part[i][mt][3], acc[i][mt][3]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) part[i][mt][q] = 0.f;
+        for (int r = 0; r < 4; ++r) part[i][mt][r] = 0.f;
       }
   };
-  bool mval[MT8];
-#pragma unroll
-  for (int mt = 0; mt < MT8; ++mt) mval[mt] = 8 * mt + g < Mr;
-  const int xlane = g * 4 + t;
-
-  for (int j = 0; j < nmine; ++j) {
-    cp_async_wait<STAGES - 2>();                     // block j has landed in this lane's slot
-    LaneWords<BITS> lw[4];
-    read_block<BITS>(lw, ring + (j % STAGES) * SLOT, lane);
-    // refill the slot read in the previous iteration
-    const int jn = j + STAGES - 1;
-    if (jn < nmine) issue_block<BITS>(ring_s + (jn % STAGES) * SLOT, a.wr, blk0 + jb0 + jn, a.Np, nrow, t, lane);
-    cp_async_commit();
-
-    const int bl = jb0 + j;
-    const int gb = bgrp[bl];
-    if (gb >= 0 && gb != cur) {
-      if (cur >= 0) flush();
-      cur = gb;
-      load_group(gb);
-    }
-    const uint2* xb = xs + (size_t)bl * 8 * Mr * 4;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (gb < 0 && (s & 1) == 0) {
-        const int gg = cg[bl * 4 + (s >> 1)];
-        if (gg != cur) {
-          if (cur >= 0) flush();
-          cur = gg;
-          load_group(gg);
-        }
-      }
-      uint2 xv[MT8];
-#pragma unroll
-      for (int mt = 0; mt < MT8; ++mt)
-        xv[mt] = mval[mt] ? xb[s * Mr * 4 + mt * 32 + xlane] : make_uint2(0u, 0u);
-      const int p0 = 4 * (s >> 1) + 2 * (s & 1);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint32_t af[4];
-        af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
-        af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
-        af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
-        af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
-#pragma unroll
-        for (int mt = 0; mt < MT8; ++mt) mma16816<T>(part[i][mt], af, xv[mt].x, xv[mt].y);
-      }
-    }
-  }
-  cp_async_wait<0>();
-  if (cur >= 0) flush();
-
-  // ---- k-group partial tiles meet in shared memory: red[kg][m][n] ----
-  {
-    float* rk = red + (size_t)kg * MT8 * 8 * RS;
+  int s_base = 0;
+  int q = 0;
+  for (int ti = T0; ti < T1; ++ti) {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
-      for (int mt = 0; mt < MT8; ++mt) {
-        const int nl = cw * 32 + 16 * i + g;
-        const int ml = 8 * mt + 2 * t;
-        rk[ml * RS + nl] = acc[i][mt][0];
-        rk[(ml + 1) * RS + nl] = acc[i][mt][1];
-        rk[ml * RS + nl + 8] = acc[i][mt][2];
-        rk[(ml + 1) * RS + nl + 8] = acc[i][mt][3];
+      for (int mt = 0; mt < MT8; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) { acc[i][mt][r] = 0.f; part[i][mt][r] = 0.f; }
+    for (int p = 0; p < a.npanel; ++p, ++q) {
+      const int nb = panel_blocks(p);
+      const int hs = q & 1;
+      if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1))) ok = false;
+      const uint8_t* xb = xreg + (a.single ? 0 : hs * x_bytes);
+      const uint8_t* zs = zsreg + hs * zs_bytes;
+      const int gf = cg[4 * p * a.pb];
+      int cur = -1;                    // group whose zeros and scales are loaded
+      const int nst = (nb + kSPB - 1) / kSPB;
+      for (int js = (warp - s_base) & (kCW - 1); js < nst && ok; js += kCW) {
+        const int s = s_base + js;
+        const int slot = s & (rd - 1);
+        if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
+        const int nu = min(kSPB, nb - kSPB * js);
+        const uint8_t* st = ring + (size_t)slot * SB;
+        for (int u = 0; u < nu; ++u) {
+          const int lb = kSPB * js + u;
+          LaneWords<BITS> lw[4];
+          read_block<BITS>(lw, st + u * BITS * 512, LO);
+          if (u == nu - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(slot));     // every word of the stage is in registers
+          }
+          const int b = p * a.pb + lb;
+          const uint8_t* xblk = xb + lb * 256;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int gq = cg[4 * b + c];
+            if (gq != cur) {
+              if (cur >= 0) flush();
+              cur = gq;
+              const uint8_t* zrow = zs + (gq - gf) * kZsRow;
+              const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
+              const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
+#pragma unroll
+              for (int idx = 0; idx < 4; ++idx) zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
+              sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
+              sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+              const int ks = 2 * c + s2;                       // 16-k step inside the block
+              uint32_t b0[MT8], b1[MT8];
+#pragma unroll
+              for (int mt = 0; mt < MT8; ++mt) {
+                const uint2 v = *reinterpret_cast<const uint2*>(xblk + xoff[mt] + 64 * c + 8 * s2);
+                b0[mt] = mval[mt] ? v.x : 0u;
+                b1[mt] = mval[mt] ? v.y : 0u;
+              }
+              const int p0 = 4 * c + 2 * s2;
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                uint32_t af[4];
+                af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
+                af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
+                af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
+                af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
+#pragma unroll
+                for (int mt = 0; mt < MT8; ++mt) mma16816<T>(part[i][mt], af, b0[mt], b1[mt]);
+              }
+            }
+          }
+        }
       }
-  }
-  __syncthreads();
-  T* y = static_cast<T*>(a.y);
-  const int S = a.splits;
-  if (S == 1) {
-    for (int i = tid; i < Mr * (NCOL / 4); i += kThreads) {
-      const int ml = i / (NCOL / 4), cl = 4 * (i % (NCOL / 4));
+      if (cur >= 0) flush();
+      s_base += nst;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hempty(hs));
+    }
+    // ---- the eight warps' partial tiles meet in shared memory: red[w][m][n] ----
+    named_sync_consumers();               // the previous tile's sums have been read
+    {
+      float* rw = red + (size_t)warp * MT8 * 8 * RS;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int mt = 0; mt < MT8; ++mt) {
+          const int nl = 16 * i + g;
+          const int ml = 8 * mt + 2 * t;
+          rw[ml * RS + nl] = acc[i][mt][0];
+          rw[(ml + 1) * RS + nl] = acc[i][mt][1];
+          rw[ml * RS + nl + 8] = acc[i][mt][2];
+          rw[(ml + 1) * RS + nl + 8] = acc[i][mt][3];
+        }
+    }
+    named_sync_consumers();
+    if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
+    T* y = static_cast<T*>(a.y);
+    for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+      const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
       float4 sum = *reinterpret_cast<const float4*>(&red[ml * RS + cl]);
 #pragma unroll
-      for (int k = 1; k < KG; ++k) {
-        const float4 v = *reinterpret_cast<const float4*>(&red[(size_t)k * MT8 * 8 * RS + ml * RS + cl]);
+      for (int w = 1; w < kCW; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(&red[(size_t)w * MT8 * 8 * RS + ml * RS + cl]);
         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
       }
-      const int n = n_cta + cl;
+      const int n = ti * kTileN + cl;
       if (n < a.N) {   // N % 32 == 0: a group of 4 columns is all in or all out
         uint2 o;
         o.x = pack2<T>(sum.x, sum.y);
         o.y = pack2<T>(sum.z, sum.w);
-        *reinterpret_cast<uint2*>(y + (size_t)(m0 + ml) * a.N + n) = o;
+        *reinterpret_cast<uint2*>(y + (size_t)ml * a.N + n) = o;
       }
     }
-    return;
   }
-  // ---- K split over the cluster: fold the k-groups, then ranks in fixed order ----
-  for (int i = tid; i < Mr * NCOL; i += kThreads) {
-    const int ml = i / NCOL, nl = i % NCOL;
-    float v = red[ml * RS + nl];
-#pragma unroll
-    for (int k = 1; k < KG; ++k) v += red[(size_t)k * MT8 * 8 * RS + ml * RS + nl];
-    red[ml * RS + nl] = v;
-  }
-  uint32_t rank;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-  const int cols = NCOL / S, c0 = (int)rank * cols;
-  for (int i = tid; i < Mr * (cols / 4); i += kThreads) {
-    const int ml = i / (cols / 4), cl = c0 + 4 * (i % (cols / 4));
-    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint32_t local = smem_u32(&red[ml * RS + cl]);
-    for (int sp = 0; sp < S; ++sp) {
-      float4 v;
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(sp));
-      asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote));
-      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-    }
-    const int n = n_cta + cl;
-    if (n < a.N) {
-      uint2 o;
-      o.x = pack2<T>(sum.x, sum.y);
-      o.y = pack2<T>(sum.z, sum.w);
-      *reinterpret_cast<uint2*>(y + (size_t)(m0 + ml) * a.N + n) = o;
-    }
-  }
-  // keep this CTA's shared memory alive until every rank has read it
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
 }
 
-struct SmallPlan { int ncw, splits, bps, mtiles, ntiles, span_max; size_t smem; int g_first[kMaxSplit]; };
-
-template <typename T, int BITS, int MT8, int NCW>
-int occupancy(int smem) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_small<T, BITS, MT8, NCW>, kThreads, smem) != cudaSuccess)
-    return 1;
-  return n > 0 ? n : 1;
+// xp[m][j] = x[m][perm[j]] (0 for pad rows): activations in sorted k order for the bulk copies.
+__global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, uint16_t* __restrict__ xp,
+                           int M, int K, int Kr) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");    // x may be the previous grid's output
+  const long total = (long)M * Kr;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / Kr), j = (int)(i % Kr);
+    const int k = __ldg(&perm[j]);
+    xp[i] = k >= 0 ? x[(size_t)m * K + k] : (uint16_t)0;
+  }
 }
 
-// Group span of each split: cgid ascends, so the groups of chunks [c0, c1) lie in
-// [cgid[c0], cgid[c1-1]].  Returns the largest span (capped at the chunk count) and fills g_first.
-int split_spans(const Handle& h, int bps, int S, int* g_first) {
+// Host plan: ints only, cached per handle and M.
+struct SmallPlan {
+  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_bar, smem;
+};
+
+template <int BITS, int MT8>
+bool make_plan(const Handle& h, int M, SmallPlan& p) {
   const int NB = h.Kr / 128;
-  int best = 1;
-  for (int sp = 0; sp < kMaxSplit; ++sp) g_first[sp] = 0;
-  for (int sp = 0; sp < S; ++sp) {
-    const int b0 = sp * bps;
-    if (b0 >= NB) continue;
-    const int c0 = 4 * b0, c1 = 4 * std::min(NB, b0 + bps);
-    g_first[sp] = h.cgid_host[c0];
-    best = std::max(best, h.cgid_host[c1 - 1] - h.cgid_host[c0] + 1);
+  p.ntiles = (h.N + kTileN - 1) / kTileN;
+  p.grid = std::min(p.ntiles, h.sm_count);
+  // K-panel: all of K when x fits, else as many blocks as kXPanel holds (x double buffered)
+  const int x_all = M * (NB * 256 + 64);
+  int target = kSmemFull;
+  if (x_all <= kXSingle) {
+    p.single = 1;
+    p.pb = NB;
+    if (x_all <= kXSmall) target = kSmemHalf;
+  } else {
+    p.single = 0;
+    p.pb = std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB);
   }
-  return std::min(best, 4 * bps);
-}
-
-template <typename T, int BITS, int MT8, int NCW>
-void consider(const Handle& h, int M, SmallPlan& best, long& best_cost) {
-  constexpr int KG = kWarps / NCW, NCOL = NCW * 32;
-  const int NB = h.Kr / 128;
-  const int mtiles = (M + MT8 * 8 - 1) / (MT8 * 8);
-  const int mrows = std::min(M, MT8 * 8);
-  const int ntiles = h.Np / NCOL;
-  for (int S = 1; S <= kMaxSplit && S <= NB; S *= 2) {
-    const int bps = (NB + S - 1) / S;
-    if (S > 1 && bps * 128 * mrows * 2 <= kXsBudget / 2) break;   // split K only to make x fit
-    if (bps * 128 * mrows * 2 > kXsBudget && S < kMaxSplit && S < NB) continue;
-    int gf[kMaxSplit];
-    const int span = split_spans(h, bps, S, gf);
-    const SmallSmem L = small_smem(slot_bytes<BITS>(), ring_stages<BITS>(), bps, mrows, span, NCOL, KG, MT8);
-    if (L.total > 227 * 1024) continue;
-    const int R = occupancy<T, BITS, MT8, NCW>(L.total);
-    const long ctas = (long)ntiles * S * mtiles;
-    const long per_sm = (ctas + h.sm_count - 1) / h.sm_count;     // CTAs on the busiest SM
-    const long waves = (ctas + (long)R * h.sm_count - 1) / ((long)R * h.sm_count);
-    const int bpw = (bps + KG - 1) / KG;
-    // cost: weight bytes the busiest SM streams (blocks x columns), one wave preferred; a small charge
-    // for long per-warp chains and for cluster splits
-    const long cost = per_sm * bps * NCW * 64 + (waves - 1) * 100000000L + (long)bpw + 8L * (S - 1);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best.ncw = NCW; best.splits = S; best.bps = bps; best.mtiles = mtiles; best.ntiles = ntiles;
-      best.span_max = span; best.smem = L.total;
-      std::copy(gf, gf + kMaxSplit, best.g_first);
-    }
+  p.npanel = (NB + p.pb - 1) / p.pb;
+  p.span_max = 1;
+  for (int q = 0; q < p.npanel; ++q) {
+    const int b0 = q * p.pb, b1 = std::min(NB, b0 + p.pb);
+    p.span_max = std::max(p.span_max, h.cgid_host[4 * b1 - 1] - h.cgid_host[4 * b0] + 1);
   }
-}
-
-template <typename T, int BITS, int MT8, int NCW>
-cudaError_t launch_kernel(const Handle& h, const SmallPlan& p, const void* x, void* y, int M, cudaStream_t st) {
-  auto kern = k_gemm_small<T, BITS, MT8, NCW>;
-  SmallArgs args{h.wr, h.perm, h.cgid, h.s_r, h.z_r, x, y, h.err, M, h.N, h.Np, h.K, h.Kr, h.G, h.identity,
-                 p.bps, p.splits, p.span_max, {}};
-  std::copy(p.g_first, p.g_first + kMaxSplit, args.g_first);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.ntiles, p.splits, p.mtiles);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = p.smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = p.splits;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = p.splits > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, args);
+  p.x_row = p.pb * 256 + 64;
+  const int x_bytes = (p.single ? 1 : 2) * M * p.x_row;
+  const int zs_bytes = 2 * p.span_max * kZsRow;
+  const int red_bytes = kCW * MT8 * 8 * (kTileN + 4) * 4;
+  const int cg_bytes = (NB * 4 * 4 + 15) / 16 * 16;
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + 4 * 8 + 16;
+  const int SB = stage_bytes<BITS>();
+  int budget = target - fixed - 128;
+  int rd = budget / (SB + 16);
+  if (rd < 4) {   // large tables: take up to a whole SM's shared memory
+    budget = kSmemFull - fixed - 128;
+    rd = budget / (SB + 16);
+  }
+  if (rd < 2) return false;
+  rd = std::min(rd, 128);
+  p.lg_rd = 0;
+  while ((2 << p.lg_rd) <= rd) ++p.lg_rd;     // largest power of two <= rd
+  const int rdp = 1 << p.lg_rd;
+  p.o_x = rdp * SB;
+  p.o_zs = p.o_x + (x_bytes + 15) / 16 * 16;
+  p.o_red = p.o_zs + zs_bytes;
+  p.o_cg = p.o_red + red_bytes;
+  p.o_bar = p.o_cg + cg_bytes;
+  p.smem = p.o_bar + (2 * rdp + 4) * 8 + 128;     // + alignment slack of the base
+  return p.smem <= 227 * 1024;
 }
 
 template <typename T, int BITS, int MT8>
 cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
+  auto kern = k_gemm_small<T, BITS, MT8>;
   SmallPlan p{};
   {
     std::lock_guard<std::mutex> lock(h.plan_mu);
     const int64_t key = ((int64_t)GPTQ_PATH_SMALL_M << 32) | (uint32_t)M;
     auto it = h.plans.find(key);
     if (it == h.plans.end()) {
-      long best_cost = -1;
-      consider<T, BITS, MT8, 1>(h, M, p, best_cost);
-      consider<T, BITS, MT8, 2>(h, M, p, best_cost);
-      consider<T, BITS, MT8, 4>(h, M, p, best_cost);
-      if (best_cost < 0) return cudaErrorInvalidConfiguration;
-      // every plan fits 227 KB; allow the kernels that much dynamic shared memory
-      for (cudaError_t e : {cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024),
-                            cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024),
-                            cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)})
-        if (e != cudaSuccess) return e;
-      std::vector<int64_t> v = {p.ncw, p.splits, p.bps, p.mtiles, p.ntiles, p.span_max, (int64_t)p.smem};
-      v.insert(v.end(), p.g_first, p.g_first + kMaxSplit);
+      if (!make_plan<BITS, MT8>(h, M, p)) return cudaErrorInvalidConfiguration;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
+      std::memcpy(v.data(), &p, sizeof(SmallPlan));
       h.plans[key] = v;
     } else {
-      const auto& v = it->second;
-      p.ncw = (int)v[0]; p.splits = (int)v[1]; p.bps = (int)v[2]; p.mtiles = (int)v[3]; p.ntiles = (int)v[4];
-      p.span_max = (int)v[5]; p.smem = (size_t)v[6];
-      for (int i = 0; i < kMaxSplit; ++i) p.g_first[i] = (int)v[7 + i];
+      std::memcpy(&p, it->second.data(), sizeof(SmallPlan));
     }
   }
-  switch (p.ncw) {
-    case 1: return launch_kernel<T, BITS, MT8, 1>(h, p, x, y, M, st);
-    case 2: return launch_kernel<T, BITS, MT8, 2>(h, p, x, y, M, st);
-    default: return launch_kernel<T, BITS, MT8, 4>(h, p, x, y, M, st);
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  int ldx = h.K;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (!h.identity) {
+    cudaLaunchConfig_t gcfg = {};
+    const long total = (long)M * h.Kr;
+    gcfg.gridDim = dim3((unsigned)std::min<long>((total + 255) / 256, 2L * h.sm_count));
+    gcfg.blockDim = dim3(256);
+    gcfg.stream = st;
+    gcfg.attrs = attr;
+    gcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&gcfg, k_gather_x, static_cast<const uint16_t*>(x), (const int32_t*)h.perm,
+                                       static_cast<uint16_t*>(h.xp), M, h.K, h.Kr);
+    if (e != cudaSuccess) return e;
+    xs = static_cast<const uint16_t*>(h.xp);
+    ldx = h.Kr;
   }
+  SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
+                 p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
+                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreadsS);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args, h.wr_map);
 }
 
 template <typename T, int BITS>
@@ -609,7 +618,7 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 
 }  // namespace
 
-int small_m_launches(const Handle&, int M) { return M > 0 ? 1 : 0; }
+int small_m_launches(const Handle& h, int M) { return M > 0 ? (h.identity ? 1 : 2) : 0; }
 
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
   if (h.dtype == GPTQ_BF16) return launch_dtype<__nv_bfloat16>(h, x, y, M, st);

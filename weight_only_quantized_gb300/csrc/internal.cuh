@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of the GPTQ library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -30,7 +31,11 @@ struct Handle {
   int32_t* cgid = nullptr;   // [Kr/32] group of each 32-row chunk
   uint16_t* s_r = nullptr;   // [G][Np] scale bits
   uint8_t* z_r = nullptr;    // [G][Np] stored zero (zero - 1)
+  uint8_t* zst = nullptr;    // [Np/32][G][96]: per 32-column tile and group, 32 stored zeros then
+                             // 32 scales, column c at position (c % 8) * 4 + c / 8 (small-M path)
   std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)
+  alignas(64) CUtensorMap wr_map;   // wr as uint64 [Kr/128 * bits rows][2 Np]: one box = kSmallBlocksPerBox
+                                    // blocks of one 32-column tile (small-M path)
   int32_t* err = nullptr;    // device error word: kernels set it when a bounded wait gives up
   // workspace
   int reserved_M = 0;
@@ -42,13 +47,33 @@ struct Handle {
   mutable std::unordered_map<int64_t, std::vector<int64_t>> plans;
 };
 
+// 128-row blocks fetched by one TMA box of the small-M kernel.
+constexpr int kSmallBlocksPerBox = 4;
+
+// Column position inside a 32-column group of the runtime codes: vector v of a block stores the
+// 16-byte word of column c (c = n % 32) at position (c + code_col_rot(bits, v)) % 32.  With
+// these rotations, the lanes of a quarter warp that read different vectors of the same columns
+// land on different shared-memory banks when a block is copied densely.
+__host__ __device__ __forceinline__ int code_col_rot(int bits, int v) {
+  return bits == 4 ? 2 * v : bits == 8 ? 2 * (v >> 1) : (bits == 2 || v < 2) ? 4 * v : 0;
+}
+__host__ __device__ __forceinline__ int code_col_pos(int bits, int v, int n) {
+  return (n & ~31) | (((n & 31) + code_col_rot(bits, v)) & 31);
+}
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+
 // Status with message, recorded per thread.
 gptq_status_t fail(gptq_status_t s, const std::string& msg);
 gptq_status_t cuda_fail(cudaError_t e, const char* what);
 
 // ---- kernels launched from the host code (defined in the .cu files) ----
 
-// Small-M path: mma.sync (swap-AB) kernel with split-K reduced inside a thread-block cluster.
+// Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
 

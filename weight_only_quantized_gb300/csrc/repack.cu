@@ -17,7 +17,10 @@
 //    A plane of bp bits per code holds F = 16/bp fields in each 16-bit half of a word; pair p
 //    lives in lane word jw = p/F, field f = p%F, at bit 16h + bp*f.  Lane t owns words
 //    q = t*bp .. t*bp + bp-1; word q sits in 16-byte vector q/4, slot q%4.  Vectors of one
-//    (block, column) are stored [B][vector][column][16 bytes], plane after plane.
+//    (block, column) are stored [B][vector][column][16 bytes], plane after plane; inside each
+//    group of 32 columns, vector V keeps column c at position (c + rot(V)) % 32 with rot = 2V
+//    (4-bit), 2 (V / 2) (8-bit), 4V (2-bit, and the 2-bit plane of 3-bit), 0 (3-bit 1-bit plane),
+//    so that lanes reading different vectors of a densely copied block use different banks.
 //    bits 2/4/8 use one plane (bp = bits); bits 3 uses a 2-bit plane (code & 3) followed by a
 //    1-bit plane (code >> 2), in the spirit of GPTQModel's planar packing (fields never
 //    straddle words), a layout chosen for the decoder, not a checkpoint format.
@@ -180,7 +183,7 @@ __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t*
       }
     out[w] = word;
   }
-  uint4* dst = reinterpret_cast<uint4*>(wr + (((size_t)B * bits + V) * Np + n) * 16);
+  uint4* dst = reinterpret_cast<uint4*>(wr + (((size_t)B * bits + V) * Np + code_col_pos(bits, V, n)) * 16);
   *dst = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
@@ -200,6 +203,23 @@ __global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __
   }
   s_r[(long)g * Np + n] = s;
   z_r[(long)g * Np + n] = z;
+  }
+}
+
+// zst[(T * G + g) * 96 + pos] = z_r[g][32 T + c] and, as 16-bit words after the 32 zero bytes,
+// s_r[g][32 T + c], with pos = (c % 8) * 4 + c / 8: the four columns c = g8 + 8 j that one lane of
+// the small-M kernel owns are adjacent.  One warp per (tile, group row range).
+__global__ void k_pack_zst(const uint16_t* __restrict__ s_r, const uint8_t* __restrict__ z_r, int Np, int G,
+                           uint8_t* __restrict__ zst) {
+  const int c = threadIdx.x & 31;
+  const int T = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (T >= Np / 32) return;
+  const int pos = (c % 8) * 4 + c / 8;
+  const long n = 32L * T + c;
+  for (int g = blockIdx.y; g < G; g += gridDim.y) {
+    uint8_t* row = zst + ((long)T * G + g) * 96;
+    row[pos] = z_r[(long)g * Np + n];
+    reinterpret_cast<uint16_t*>(row + 32)[pos] = s_r[(long)g * Np + n];
   }
 }
 
@@ -238,9 +258,25 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   if ((e = cudaMalloc(&h.wr, wr_b)) != cudaSuccess || (e = cudaMalloc(&h.perm, sizeof(int32_t) * h.Kr)) != cudaSuccess ||
       (e = cudaMalloc(&h.cgid, sizeof(int32_t) * (h.Kr / 32))) != cudaSuccess ||
       (e = cudaMalloc(&h.s_r, sizeof(uint16_t) * (size_t)G * h.Np)) != cudaSuccess ||
-      (e = cudaMalloc(&h.z_r, (size_t)G * h.Np)) != cudaSuccess) {
+      (e = cudaMalloc(&h.z_r, (size_t)G * h.Np)) != cudaSuccess ||
+      (e = cudaMalloc(&h.zst, (size_t)G * h.Np * 3)) != cudaSuccess) {
     cleanup();
     return cuda_fail(e, "cudaMalloc(runtime layout)");
+  }
+  {
+    // the small-M kernel's view of wr: uint64 [Kr/128 * bits rows][2 Np], one box = four blocks
+    // of one 32-column tile (4 * bits rows of 512 bytes)
+    EncodeTiledFn enc = encode_fn();
+    const cuuint64_t dims[2] = {(cuuint64_t)h.Np * 2, (cuuint64_t)(h.Kr / 128) * h.bits};
+    const cuuint64_t strides[1] = {(cuuint64_t)h.Np * 16};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(kSmallBlocksPerBox * h.bits)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (!enc || enc(&h.wr_map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, h.wr, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      cleanup();
+      return fail(GPTQ_ERR_CUDA, "cuTensorMapEncodeTiled(runtime codes) failed");
+    }
   }
   if ((e = cudaMemsetAsync(cursor, 0, sizeof(int32_t) * G, st)) != cudaSuccess) { cleanup(); return cuda_fail(e, "memset"); }
   k_scatter_perm<<<1, 32, 0, st>>>(g_idx, K, h.group_size, off, cursor, h.perm);
@@ -250,6 +286,8 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, h.wr);
   dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
   k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, h.s_r, h.z_r);
+  dim3 gz(h.Np / 32 / 8, G < 65535 ? G : 65535);
+  k_pack_zst<<<gz, 256, 0, st>>>(h.s_r, h.z_r, h.Np, G, h.zst);
   if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
   h.cgid_host.resize(h.Kr / 32);
   if ((e = cudaMemcpyAsync(h.cgid_host.data(), h.cgid, sizeof(int32_t) * (h.Kr / 32), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
