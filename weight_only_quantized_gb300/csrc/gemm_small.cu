@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
   // Let the next grid on the stream launch; it waits for this one before touching our outputs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
-    for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), 1); }
+    for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), kSPB); }
     for (int i = 0; i < 2; ++i) { mbar_init(hfull(i), 1); mbar_init(hempty(i), kCW); }
     fence_mbar_init();
   }
@@ -384,36 +384,39 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
       const int gf = cg[4 * p * a.pb];
       int cur = -1;                    // group whose zeros and scales are loaded
       const int nst = (nb + kSPB - 1) / kSPB;
-      for (int js = (warp - s_base) & (kCW - 1); js < nst && ok; js += kCW) {
+      // block slot bs = kSPB * js + u of stage js goes to warp (kSPB * (s_base + js) + u) % kCW;
+      // every slot's owner releases it once, also past the last block (the stage's empty barrier
+      // counts kSPB arrivals)
+      for (int bs = (warp - kSPB * s_base) & (kCW - 1); bs < kSPB * nst && ok; bs += kCW) {
+        const int js = bs / kSPB, u = bs % kSPB;
         const int s = s_base + js;
         const int slot = s & (rd - 1);
         if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
-        const int nu = min(kSPB, nb - kSPB * js);
-        const uint8_t* st = ring + (size_t)slot * SB;
-        for (int u = 0; u < nu; ++u) {
-          const int lb = kSPB * js + u;
+        const int lb = bs;
+        if (lb >= nb) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(slot));
+          continue;
+        }
+        {
           LaneWords<BITS> lw[4];
-          read_block<BITS>(lw, st + u * BITS * 512, LO);
-          if (u == nu - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(slot));     // every word of the stage is in registers
-          }
+          read_block<BITS>(lw, ring + (size_t)slot * SB + u * BITS * 512, LO);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(slot));       // this block's words are in registers
           const int b = p * a.pb + lb;
           const uint8_t* xblk = xb + lb * 256;
+          auto load_group = [&](int gq) {
+            if (cur >= 0) flush();
+            cur = gq;
+            const uint8_t* zrow = zs + (gq - gf) * kZsRow;
+            const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
+            const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int gq = cg[4 * b + c];
-            if (gq != cur) {
-              if (cur >= 0) flush();
-              cur = gq;
-              const uint8_t* zrow = zs + (gq - gf) * kZsRow;
-              const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
-              const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
-#pragma unroll
-              for (int idx = 0; idx < 4; ++idx) zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
-              sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
-              sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
-            }
+            for (int idx = 0; idx < 4; ++idx) zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
+            sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
+            sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+          };
+          auto chunk_mma = [&](const int c) {
 #pragma unroll
             for (int s2 = 0; s2 < 2; ++s2) {
               const int ks = 2 * c + s2;                       // 16-k step inside the block
@@ -435,6 +438,20 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt) mma16816<T>(part[i][mt], af, b0[mt], b1[mt]);
               }
+            }
+          };
+          const int g0 = cg[4 * b], g3 = cg[4 * b + 3];
+          if (g0 == g3) {
+            // one group for the whole block (cgid ascends): no branch between the chunks
+            if (g0 != cur) load_group(g0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) chunk_mma(c);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int gq = cg[4 * b + c];
+              if (gq != cur) load_group(gq);
+              chunk_mma(c);
             }
           }
         }
