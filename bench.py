@@ -333,7 +333,7 @@ def run_native(args, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                     "kernel": "k_gemm_small (small-M, mma.sync swap-AB, cluster split-K)",
+                     "kernel": "k_gemm_small (small-M: persistent TMA-fed weight stream, mma.sync swap-AB)",
                      "timing": "CUDA events around one replay of a graph of the timed calls"},
         "eager_us_per_call": round(eager * 1e6, 3),
         "e2e": {"value": round(B * ws / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": 2 * M * spec.K,

@@ -529,7 +529,9 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   if (x_all <= kXSingle) {
     p.single = 1;
     p.pb = NB;
-    if (x_all <= kXSmall) target = kSmemHalf;
+    // half an SM (a second CTA of the next call can start streaming) only for short runs of tiles;
+    // longer runs want the deeper ring
+    if (x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3) target = kSmemHalf;
   } else {
     p.single = 0;
     p.pb = std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB);
