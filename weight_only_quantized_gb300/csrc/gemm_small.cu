@@ -131,6 +131,16 @@ __device__ __forceinline__ uint32_t prep_zero(uint32_t stored) {
   else return (Magic<T>::bits + z) * 0x00010001u;                                   // magic + z, both halves
 }
 
+// Codes go into the MMA as the exact values magic + code (bf16 128 + q, fp16 1024 + q) and the
+// zero is taken out once per group in fp32: sum_k x (q - z) = sum_k x (magic + q) - (magic + z) sum_k x,
+// with sum_k x from one extra MMA against an all-ones operand.  Products stay exact; the
+// subtraction cancels at most ~11 of fp32's 24 bits, far inside the 4e-3 relative budget, and the
+// per-pair packed subtract (half-rate fp16 pipe) disappears.  Not for 8-bit codes with bf16, whose
+// 128 + q is not exact.
+template <typename T, int BITS> constexpr bool kFoldZero = !kViaF32<T, BITS>;
+template <typename T> constexpr float kMagicF = std::is_same<T, __nv_bfloat16>::value ? 128.0f : 1024.0f;
+template <typename T> constexpr uint32_t kOnes2 = std::is_same<T, __nv_bfloat16>::value ? 0x3F803F80u : 0x3C003C00u;
+
 // Lane words of one (block, column) for this lane: BITS words (bits 3: 2 words of the 2-bit plane
 // then 1 word of the 1-bit plane).
 template <int BITS> struct LaneWords { uint32_t w[BITS]; };
@@ -153,6 +163,21 @@ __device__ __forceinline__ uint32_t operand(const LaneWords<BITS>& lw, int p, ui
     constexpr int F = 16 / BITS;
     constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
     return sub2<T>(and_or(lw.w[p / F] >> (BITS * (p % F)), mask, M2), zq);
+  }
+}
+
+// magic + code of pair p (both halves), exact (the kFoldZero form).
+template <typename T, int BITS>
+__device__ __forceinline__ uint32_t operand_raw(const LaneWords<BITS>& lw, int p) {
+  constexpr uint32_t M2 = Magic<T>::bits * 0x00010001u;
+  if constexpr (BITS == 3) {
+    const uint32_t lo = and_or(lw.w[p / 8] >> (2 * (p % 8)), 0x00030003u, M2);
+    const uint32_t hi = p <= 2 ? (lw.w[2] << (2 - p)) : (lw.w[2] >> (p - 2));
+    return and_or(hi, 0x00040004u, lo);
+  } else {
+    constexpr int F = 16 / BITS;
+    constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
+    return and_or(lw.w[p / F] >> (BITS * (p % F)), mask, M2);
   }
 }
 
@@ -342,6 +367,7 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
   bool ok = true;
   bool waited = false;
   float acc[2][MT8][4], part[2][MT8][4];
+  float xsp[MT8][4];               // kFoldZero: sum of x over the group so far (c0: column 2t, c1: 2t + 1)
   bool mval[MT8];
 #pragma unroll
   for (int mt = 0; mt < MT8; ++mt) mval[mt] = 8 * mt + g < a.M;
@@ -351,20 +377,32 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
   int xoff[MT8];
 #pragma unroll
   for (int mt = 0; mt < MT8; ++mt) xoff[mt] = (mval[mt] ? 8 * mt + g : 0) * a.x_row + 16 * t;
-  uint32_t zq[4];
+  uint32_t zq[4];                  // prepared zero (the subtract form)
+  float zc[4];                     // magic + zero in fp32 (the kFoldZero form)
   float sc[4];
   auto flush = [&]() {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
       for (int mt = 0; mt < MT8; ++mt) {
-        acc[i][mt][0] = fmaf(sc[2 * i], part[i][mt][0], acc[i][mt][0]);
-        acc[i][mt][1] = fmaf(sc[2 * i], part[i][mt][1], acc[i][mt][1]);
-        acc[i][mt][2] = fmaf(sc[2 * i + 1], part[i][mt][2], acc[i][mt][2]);
-        acc[i][mt][3] = fmaf(sc[2 * i + 1], part[i][mt][3], acc[i][mt][3]);
+        if constexpr (kFoldZero<T, BITS>) {
+          acc[i][mt][0] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsp[mt][0], part[i][mt][0]), acc[i][mt][0]);
+          acc[i][mt][1] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsp[mt][1], part[i][mt][1]), acc[i][mt][1]);
+          acc[i][mt][2] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsp[mt][0], part[i][mt][2]), acc[i][mt][2]);
+          acc[i][mt][3] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsp[mt][1], part[i][mt][3]), acc[i][mt][3]);
+        } else {
+          acc[i][mt][0] = fmaf(sc[2 * i], part[i][mt][0], acc[i][mt][0]);
+          acc[i][mt][1] = fmaf(sc[2 * i], part[i][mt][1], acc[i][mt][1]);
+          acc[i][mt][2] = fmaf(sc[2 * i + 1], part[i][mt][2], acc[i][mt][2]);
+          acc[i][mt][3] = fmaf(sc[2 * i + 1], part[i][mt][3], acc[i][mt][3]);
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) part[i][mt][r] = 0.f;
       }
+#pragma unroll
+    for (int mt = 0; mt < MT8; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) xsp[mt][r] = 0.f;
   };
   int s_base = 0;
   int q = 0;
@@ -374,7 +412,7 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
 #pragma unroll
       for (int mt = 0; mt < MT8; ++mt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) { acc[i][mt][r] = 0.f; part[i][mt][r] = 0.f; }
+        for (int r = 0; r < 4; ++r) { acc[i][mt][r] = 0.f; part[i][mt][r] = 0.f; xsp[mt][r] = 0.f; }
     for (int p = 0; p < a.npanel; ++p, ++q) {
       const int nb = panel_blocks(p);
       const int hs = q & 1;
@@ -412,31 +450,46 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
             const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
             const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
 #pragma unroll
-            for (int idx = 0; idx < 4; ++idx) zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
+            for (int idx = 0; idx < 4; ++idx) {
+              const uint32_t zst8 = (zw >> (8 * idx)) & 0xFFu;
+              if constexpr (kFoldZero<T, BITS>) zc[idx] = kMagicF<T> + (float)(zst8 + 1u);
+              else zq[idx] = prep_zero<T, BITS>(zst8);
+            }
             sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
             sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
           };
           auto chunk_mma = [&](const int c) {
+            // both 16-k steps of the chunk: one 16-byte load per m-tile (lanes of absent rows read
+            // row 0; their columns of the product are never stored)
+            uint4 xv[MT8];
+#pragma unroll
+            for (int mt = 0; mt < MT8; ++mt) xv[mt] = *reinterpret_cast<const uint4*>(xblk + xoff[mt] + 64 * c);
 #pragma unroll
             for (int s2 = 0; s2 < 2; ++s2) {
-              const int ks = 2 * c + s2;                       // 16-k step inside the block
-              uint32_t b0[MT8], b1[MT8];
-#pragma unroll
-              for (int mt = 0; mt < MT8; ++mt) {
-                const uint2 v = *reinterpret_cast<const uint2*>(xblk + xoff[mt] + 64 * c + 8 * s2);
-                b0[mt] = mval[mt] ? v.x : 0u;
-                b1[mt] = mval[mt] ? v.y : 0u;
-              }
               const int p0 = 4 * c + 2 * s2;
 #pragma unroll
               for (int i = 0; i < 2; ++i) {
                 uint32_t af[4];
-                af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
-                af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
-                af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
-                af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
+                if constexpr (kFoldZero<T, BITS>) {
+                  af[0] = operand_raw<T, BITS>(lw[2 * i], p0);
+                  af[1] = operand_raw<T, BITS>(lw[2 * i + 1], p0);
+                  af[2] = operand_raw<T, BITS>(lw[2 * i], p0 + 1);
+                  af[3] = operand_raw<T, BITS>(lw[2 * i + 1], p0 + 1);
+                } else {
+                  af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
+                  af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
+                  af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
+                  af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
+                }
 #pragma unroll
-                for (int mt = 0; mt < MT8; ++mt) mma16816<T>(part[i][mt], af, b0[mt], b1[mt]);
+                for (int mt = 0; mt < MT8; ++mt)
+                  mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+              }
+              if constexpr (kFoldZero<T, BITS>) {
+                const uint32_t ones[4] = {kOnes2<T>, kOnes2<T>, kOnes2<T>, kOnes2<T>};
+#pragma unroll
+                for (int mt = 0; mt < MT8; ++mt)
+                  mma16816<T>(xsp[mt], ones, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
               }
             }
           };
