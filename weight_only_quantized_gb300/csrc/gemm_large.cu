@@ -13,9 +13,9 @@
 // kernel, inside the k reduction.
 //
 // Design on sm_103a, one CTA per tile of 128 output features x 256 rows of x (swap-AB: D[n][m]):
-//  * warp 0: producer.  cp.async.bulk copies of the packed 128-row blocks of the tile's 128
-//    columns, and TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of 256 x 64 x tiles, each into
-//    a ring tracked by mbarriers.
+//  * warp 0: x producer, TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of 256 x 64 x tiles;
+//    warp 2: code producer, cp.async.bulk copies of each packed 128-row block of the tile's 128
+//    columns plus the stored zeros of its four chunks; each into a ring tracked by mbarriers.
 //  * warps 4..7: dequantisers, one per SM sub-partition.  Thread d owns weight row n0 + d: one LOP3
 //    per code pair makes magic + code, one packed subtract of (magic + zero) leaves the exact
 //    integer code - zero, and the row is written in the UMMA K-major SWIZZLE_128B layout (16-byte
@@ -40,7 +40,7 @@ namespace gptq {
 namespace {
 
 constexpr int BN = 128, BMX = 256, HK = 64;   // weight rows (MMA M), x rows (MMA N), k per stage
-// Four warpgroups: {producer, MMA issuer, two spare}, four dequantisers (one per SM sub-partition),
+// Four warpgroups: {x producer, MMA issuer, code producer, spare}, four dequantisers (one per SM sub-partition),
 // and eight scalers (two per TMEM lane quarter, 128 fp32 sums a thread).  setmaxnreg moves
 // registers from the first two warpgroups to the scalers: 2 x 128 x (72 + 184) = 65536.
 constexpr int kDqWarps = 4, kScWarps = 8;
@@ -48,12 +48,16 @@ constexpr int kDqWarp0 = 4, kScWarp0 = 8;
 constexpr int kThreadsL = 512;
 constexpr int kRegsLaunch = 128, kRegsLight = 72, kRegsScaler = 184;
 static_assert(2 * 128 * (kRegsLight + kRegsScaler) <= kThreadsL * kRegsLaunch, "register split exceeds the launch");
-constexpr int PS = 2, XS = 3, WS = 3;
+constexpr int XS = 3, WS = 3;
 constexpr int X_BYTES = BMX * HK * 2;           // 32 KB
 constexpr int W_BYTES = BN * HK * 2;            // 16 KB
 constexpr int kTmemCols = 512;                  // two partial-sum buffers of 256 columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 template <int BITS> constexpr int PK_BYTES = BN * 16 * BITS;  // one 128-row block of 128 columns
+// A packed stage: the block's codes, then the stored zero of each of its four 32-row chunks for the
+// tile's 128 columns (copied by the producer, so the dequant warps never wait on global loads).
+template <int BITS> constexpr int PKS_BYTES = PK_BYTES<BITS> + 4 * BN;
+template <int BITS> constexpr int PSB = BITS == 8 ? 3 : 4;     // packed stages in the ring
 
 template <typename T> struct MagicL;
 template <> struct MagicL<__half> { static constexpr uint32_t bits = 0x6400u; };
@@ -65,8 +69,8 @@ template <int BITS> struct LargeSmem {
   static constexpr int x = 0;
   static constexpr int w = x + XS * X_BYTES;
   static constexpr int pk = w + WS * W_BYTES;
-  static constexpr int bars = pk + PS * PK_BYTES<BITS>;
-  static constexpr int nbars = 2 * XS + 2 * WS + 2 * PS + 5;
+  static constexpr int bars = pk + PSB<BITS> * PKS_BYTES<BITS>;
+  static constexpr int nbars = 2 * XS + 2 * WS + 2 * PSB<BITS> + 5;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int cg = tmem_slot + 16;       // int32 group of every 32-row chunk, then one
                                                   // uint32 group-end mask per 32 chunks
@@ -210,7 +214,8 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, const __grid_constant__ CUtensorMap tmap_x) {
   using S = LargeSmem<BITS>;
-  constexpr int PKB = PK_BYTES<BITS>;
+  constexpr int PKB = PKS_BYTES<BITS>;
+  constexpr int PS = PSB<BITS>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -324,9 +329,28 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsLight));
     if (warp == 0) {
-      // ---------------- producer ----------------
+      // ---------------- x producer: TMA tiles of x ----------------
       if (lane == 0) {
-        int pk_issued = 0, x_issued = 0;
+        int x_issued = 0;
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // x may come from the previous grid
+        for (int i = 0; i < nhalf && ok; ++i) {
+          const int xs = i % XS;
+          if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(x_full(xs), X_BYTES);
+          tma_load_2d(xs_s + xs * X_BYTES, &tmap_x, i * HK, m0, x_full(xs));
+          ++x_issued;
+        }
+        // every issued copy must land before the CTA may exit
+        for (int i = x_issued > XS ? x_issued - XS : 0; i < x_issued; ++i)
+          if (!mbar_wait(x_full(i % XS), (i / XS) & 1)) ok = false;
+        if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+      }
+    } else if (warp == 2) {
+      // ---------------- packed-code producer: codes and stored zeros of each block ----------------
+      // (its own warp, so the code ring runs ahead of the x ring; handle-owned data, no wait on
+      // the previous grid)
+      if (lane == 0) {
+        int pk_issued = 0;
         for (int blk = 0; blk < nblocks && ok; ++blk) {
           const int ps = blk % PS;
           if (blk >= PS && !mbar_wait(pk_empty(ps), ((blk / PS) - 1) & 1)) { ok = false; break; }
@@ -335,21 +359,14 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   #pragma unroll
           for (int v = 0; v < BITS; ++v)
             bulk_g2s(smem_u32(pk + ps * PKB + v * BN * 16), src + (size_t)v * a.Np * 16, BN * 16, pk_full(ps));
+  #pragma unroll
+          for (int c = 0; c < 4; ++c)     // stored zeros of the block's chunks, 128 columns each
+            bulk_g2s(smem_u32(pk + ps * PKB + PK_BYTES<BITS> + c * BN), a.z_r + (size_t)cg[4 * blk + c] * a.Np + n0,
+                     BN, pk_full(ps));
           ++pk_issued;
-          if (blk == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // x may come from the previous grid
-          for (int h = 0; h < 2; ++h) {
-            const int i = 2 * blk + h, xs = i % XS;
-            if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
-            mbar_arrive_expect_tx(x_full(xs), X_BYTES);
-            tma_load_2d(xs_s + xs * X_BYTES, &tmap_x, i * HK, m0, x_full(xs));
-            ++x_issued;
-          }
         }
-        // every issued copy must land before the CTA may exit
         for (int b = pk_issued > PS ? pk_issued - PS : 0; b < pk_issued; ++b)
           if (!mbar_wait(pk_full(b % PS), (b / PS) & 1)) ok = false;
-        for (int i = x_issued > XS ? x_issued - XS : 0; i < x_issued; ++i)
-          if (!mbar_wait(x_full(i % XS), (i / XS) & 1)) ok = false;
         if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
       }
     } else if (warp == 1) {
@@ -409,19 +426,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
       // ---------------- dequantisers: thread owns weight row n0 + nrow ----------------
       const int nrow = 32 * (warp - kDqWarp0) + lane;
-      const size_t zcol = (size_t)n0 + nrow;
       uint32_t zq[4];
-      auto load_zeros = [&](int blk, uint32_t (&z)[4]) {
-  #pragma unroll
-        for (int c = 0; c < 4; ++c) z[c] = prep_zero_l<T, BITS>(__ldg(&a.z_r[(size_t)cg[blk * 4 + c] * a.Np + zcol]));
-      };
-      if (nblocks > 0) load_zeros(0, zq);
       for (int blk = 0; blk < nblocks && ok; ++blk) {
         const int ps = blk % PS;
         if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
         const uint8_t* stage = pk + ps * PKB;
-        uint32_t zn[4];
-        if (blk + 1 < nblocks) load_zeros(blk + 1, zn);     // next block's zeros, ahead of use
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) zq[c] = prep_zero_l<T, BITS>(stage[PK_BYTES<BITS> + c * BN + nrow]);
         for (int h = 0; h < 2; ++h) {
           const int i = 2 * blk + h, ws = i % WS;
           if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
@@ -449,10 +460,6 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(pk_empty(ps));           // both halves of this block are written
-        if (blk + 1 < nblocks) {
-  #pragma unroll
-          for (int c = 0; c < 4; ++c) zq[c] = zn[c];
-        }
       }
       if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
     }
