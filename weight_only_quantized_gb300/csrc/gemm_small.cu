@@ -41,8 +41,10 @@
 namespace gptq {
 namespace {
 
-constexpr int kCW = 8;                       // consumer warps
-constexpr int kThreadsS = (kCW + 1) * 32;    // + one producer warp
+// Consumer warps CW: 16 when a CTA streams a long run of tiles (the dequant chains are
+// latency-bound and more warps hide more), 8 when the CTA is short and should leave room on the SM
+// for the next call's CTA, and 8 at M > 8 (twice the accumulators).  Plus one producer warp.
+template <int CW> __host__ __device__ constexpr int threads_of() { return (CW + 1) * 32; }
 constexpr int kTileN = 32;                   // output features per tile
 constexpr int kZsRow = 96;                   // bytes of one (tile, group) row of zst
 constexpr int kSmemHalf = 110 * 1024;        // two CTAs (consecutive calls) share an SM
@@ -245,12 +247,15 @@ struct SmallArgs {
   int o_x, o_zs, o_red, o_cg, o_bar;   // shared-memory offsets; the ring starts at 0
 };
 
+template <int CW>
 __device__ __forceinline__ void named_sync_consumers() {
-  asm volatile("bar.sync 1, %0;" :: "n"(kCW * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
 }
 
-template <typename T, int BITS, int MT8>
-__global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
+template <typename T, int BITS, int MT8, int CW>
+__global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
+  constexpr int kCW = CW;
+  constexpr int kThreadsS = threads_of<CW>();
   constexpr int SB = stage_bytes<BITS>();
   constexpr int RS = kTileN + 4;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -515,7 +520,7 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
       if (lane == 0) mbar_arrive(hempty(hs));
     }
     // ---- the eight warps' partial tiles meet in shared memory: red[w][m][n] ----
-    named_sync_consumers();               // the previous tile's sums have been read
+    named_sync_consumers<kCW>();               // the previous tile's sums have been read
     {
       float* rw = red + (size_t)warp * MT8 * 8 * RS;
 #pragma unroll
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsS, MT8 == 1 ? 2 : 1) k_gemm_small(cons
           rw[(ml + 1) * RS + nl + 8] = acc[i][mt][3];
         }
     }
-    named_sync_consumers();
+    named_sync_consumers<kCW>();
     if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
     T* y = static_cast<T*>(a.y);
     for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
@@ -568,7 +573,7 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
-  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_bar, smem;
+  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_bar, smem, cw;
 };
 
 template <int BITS, int MT8>
@@ -579,12 +584,15 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   // K-panel: all of K when x fits, else as many blocks as kXPanel holds (x double buffered)
   const int x_all = M * (NB * 256 + 64);
   int target = kSmemFull;
+  // A short CTA (x small, at most three tiles) takes half an SM and 8 consumer warps, so the next
+  // call's CTA can start streaming beside it; a long one takes the whole SM, a deeper ring and
+  // (at M <= 8) 16 consumer warps.
+  const bool short_cta = x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3;
+  p.cw = (MT8 == 1 && !short_cta) ? 16 : 8;
   if (x_all <= kXSingle) {
     p.single = 1;
     p.pb = NB;
-    // half an SM (a second CTA of the next call can start streaming) only for short runs of tiles;
-    // longer runs want the deeper ring
-    if (x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3) target = kSmemHalf;
+    if (short_cta) target = kSmemHalf;
   } else {
     p.single = 0;
     p.pb = std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB);
@@ -598,7 +606,7 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   p.x_row = p.pb * 256 + 64;
   const int x_bytes = (p.single ? 1 : 2) * M * p.x_row;
   const int zs_bytes = 2 * p.span_max * kZsRow;
-  const int red_bytes = kCW * MT8 * 8 * (kTileN + 4) * 4;
+  const int red_bytes = p.cw * MT8 * 8 * (kTileN + 4) * 4;
   const int cg_bytes = (NB * 4 * 4 + 15) / 16 * 16;
   const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + 4 * 8 + 16;
   const int SB = stage_bytes<BITS>();
@@ -624,7 +632,6 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
 
 template <typename T, int BITS, int MT8>
 cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  auto kern = k_gemm_small<T, BITS, MT8>;
   SmallPlan p{};
   {
     std::lock_guard<std::mutex> lock(h.plan_mu);
@@ -632,7 +639,9 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
     auto it = h.plans.find(key);
     if (it == h.plans.end()) {
       if (!make_plan<BITS, MT8>(h, M, p)) return cudaErrorInvalidConfiguration;
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if constexpr (MT8 == 1)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if (e != cudaSuccess) return e;
       std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
       std::memcpy(v.data(), &p, sizeof(SmallPlan));
@@ -665,12 +674,14 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kThreadsS);
+  cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args, h.wr_map);
+  if constexpr (MT8 == 1)
+    if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16>, args, h.wr_map);
+  return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8>, args, h.wr_map);
 }
 
 template <typename T, int BITS>
