@@ -78,6 +78,20 @@ template <> __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&c)[4
                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A * B (no accumulator input): the first MMA of a block's partial sums.
+template <typename T>
+__device__ __forceinline__ void mma16816_z(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  const float z = 0.f;
+  if constexpr (std::is_same<T, __half>::value)
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+                 : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+  else
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+                 : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+
 template <typename T> __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b);
 template <> __device__ __forceinline__ uint32_t sub2<__half>(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   uint32_t zq[4];                  // prepared zero (the subtract form)
   float zc[4];                     // magic + zero in fp32 (the kFoldZero form)
   float sc[4];
-  auto flush = [&]() {
+  auto flush = [&](const bool rezero) {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -401,13 +415,15 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           acc[i][mt][2] = fmaf(sc[2 * i + 1], part[i][mt][2], acc[i][mt][2]);
           acc[i][mt][3] = fmaf(sc[2 * i + 1], part[i][mt][3], acc[i][mt][3]);
         }
+        if (rezero)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) part[i][mt][r] = 0.f;
+          for (int r = 0; r < 4; ++r) part[i][mt][r] = 0.f;
       }
+    if (rezero)
 #pragma unroll
-    for (int mt = 0; mt < MT8; ++mt)
+      for (int mt = 0; mt < MT8; ++mt)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) xsp[mt][r] = 0.f;
+        for (int r = 0; r < 4; ++r) xsp[mt][r] = 0.f;
   };
   int s_base = 0;
   int q = 0;
@@ -449,7 +465,6 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           const int b = p * a.pb + lb;
           const uint8_t* xblk = xb + lb * 256;
           auto load_group = [&](int gq) {
-            if (cur >= 0) flush();
             cur = gq;
             const uint8_t* zrow = zs + (gq - gf) * kZsRow;
             const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
@@ -463,7 +478,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
             sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
           };
-          auto chunk_mma = [&](const int c) {
+          auto chunk_mma = [&](const int c, const bool first) {
             // both 16-k steps of the chunk: one 16-byte load per m-tile (lanes of absent rows read
             // row 0; their columns of the product are never stored)
             uint4 xv[MT8];
@@ -487,34 +502,48 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
                   af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
                 }
 #pragma unroll
-                for (int mt = 0; mt < MT8; ++mt)
-                  mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                for (int mt = 0; mt < MT8; ++mt) {
+                  if (first && s2 == 0) mma16816_z<T>(part[i][mt], af, xv[mt].x, xv[mt].y);
+                  else mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                }
               }
               if constexpr (kFoldZero<T, BITS>) {
                 const uint32_t ones[4] = {kOnes2<T>, kOnes2<T>, kOnes2<T>, kOnes2<T>};
 #pragma unroll
-                for (int mt = 0; mt < MT8; ++mt)
-                  mma16816<T>(xsp[mt], ones, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                for (int mt = 0; mt < MT8; ++mt) {
+                  if (first && s2 == 0) mma16816_z<T>(xsp[mt], ones, xv[mt].x, xv[mt].y);
+                  else mma16816<T>(xsp[mt], ones, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                }
               }
             }
           };
+          // Every block's partial sums are folded into the total at the block's end (per block or
+          // per group change, the sum of scaled partials is the same), so no state crosses blocks.
           const int g0 = cg[4 * b], g3 = cg[4 * b + 3];
           if (g0 == g3) {
-            // one group for the whole block (cgid ascends): no branch between the chunks
+            // one group for the whole block (cgid ascends): no branch between the chunks; the first
+            // MMA starts the partial sums from zero
             if (g0 != cur) load_group(g0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) chunk_mma(c);
+            for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0);
+            flush(false);
           } else {
+            bool pending = false;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int gq = cg[4 * b + c];
-              if (gq != cur) load_group(gq);
-              chunk_mma(c);
+              if (gq != cur) {
+                if (pending) flush(false);
+                load_group(gq);
+                pending = false;
+              }
+              chunk_mma(c, !pending);
+              pending = true;
             }
+            flush(false);
           }
         }
       }
-      if (cur >= 0) flush();
       s_base += nst;
       __syncwarp();
       if (lane == 0) mbar_arrive(hempty(hs));
