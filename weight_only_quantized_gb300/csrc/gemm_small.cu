@@ -239,10 +239,18 @@ __device__ __forceinline__ void read_block(LaneWords<BITS> (&lw)[4], const uint8
   }
 }
 
-// One 2-D TMA box (global -> this CTA's shared memory), completing its bytes on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
-  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-               :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+// One 2-D TMA box (global -> this CTA's shared memory), completing its bytes on an mbarrier, with
+// an L2 cache policy (the weight stream is read once per call: evict first, so that it does not
+// push the activations, tables and outputs that the next calls reuse out of L2).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+               :: "r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(policy) : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Launch parameters (one plan per handle and M, cached on the host).
@@ -314,6 +322,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     // copies branches on a shared-memory value: the waits only poison the limit (an early-exit
     // branch on a wait result made each issue wait for the previous copy, ~4x slower here).
     uint32_t go = elect_one();
+    const uint64_t stream_policy = l2_evict_first();
     uint64_t limit = kWaitNs;
     bool waited = false;            // griddepcontrol.wait done (x may be the previous grid's output)
     int s_issued = 0;               // weight stages issued
@@ -346,7 +355,8 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             mbar_arrive_expect_tx(full(slot), (uint32_t)SB);
             // box: the kSPB * BITS vector rows from block p * pb + kSPB * l on, tile ti's 512 bytes
             // (64 uint64) of each; rows past the last block read as zero
-            tma_load_2d(smem_u32(ring + (size_t)slot * SB), &wmap, ti * 64, (p * a.pb + kSPB * l) * BITS, full(slot));
+            tma_load_2d(smem_u32(ring + (size_t)slot * SB), &wmap, ti * 64, (p * a.pb + kSPB * l) * BITS, full(slot),
+                        stream_policy);
           }
           s_sent += go ? 1 : 0;
           ++s_issued;
@@ -471,9 +481,13 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
 #pragma unroll
             for (int idx = 0; idx < 4; ++idx) {
-              const uint32_t zst8 = (zw >> (8 * idx)) & 0xFFu;
-              if constexpr (kFoldZero<T, BITS>) zc[idx] = kMagicF<T> + (float)(zst8 + 1u);
-              else zq[idx] = prep_zero<T, BITS>(zst8);
+              if constexpr (kFoldZero<T, BITS>) {
+                // magic + stored zero + 1 in fp32: one byte permute builds 2^23 + stored (exact),
+                // one add moves it (exact: integers below 2^24)
+                zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - (8388608.0f - kMagicF<T> - 1.0f);
+              } else {
+                zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
+              }
             }
             sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
             sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
