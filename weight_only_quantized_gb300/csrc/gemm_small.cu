@@ -267,6 +267,7 @@ struct SmallArgs {
   int span_max;     // rows of a zero/scale table (groups of one panel)
   int x_row;        // bytes of one staged x row: pb * 256 + 64 (rows 64 bytes apart mod 128)
   int o_x, o_zs, o_red, o_cg, o_bar;   // shared-memory offsets; the ring starts at 0
+  int o_xs;         // x sums of the single-group blocks [NB][8 MT8] (fp32)
 };
 
 template <int CW>
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   uint8_t* xreg = smem + a.o_x;
   uint8_t* zsreg = smem + a.o_zs;
   float* red = reinterpret_cast<float*>(smem + a.o_red);
+  float* xsb = reinterpret_cast<float*>(smem + a.o_xs);
   int32_t* cg = reinterpret_cast<int32_t*>(smem + a.o_cg);
   const uint32_t bar0 = smem_u32(smem + a.o_bar);
   auto full = [&](int i) { return bar0 + 8u * i; };
@@ -409,16 +411,18 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   uint32_t zq[4];                  // prepared zero (the subtract form)
   float zc[4];                     // magic + zero in fp32 (the kFoldZero form)
   float sc[4];
+  // x sums of this lane's two batch columns (8 mt + 2t and + 1) over the chunks being folded
+  float2 xsv[MT8];
   auto flush = [&](const bool rezero) {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
       for (int mt = 0; mt < MT8; ++mt) {
         if constexpr (kFoldZero<T, BITS>) {
-          acc[i][mt][0] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsp[mt][0], part[i][mt][0]), acc[i][mt][0]);
-          acc[i][mt][1] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsp[mt][1], part[i][mt][1]), acc[i][mt][1]);
-          acc[i][mt][2] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsp[mt][0], part[i][mt][2]), acc[i][mt][2]);
-          acc[i][mt][3] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsp[mt][1], part[i][mt][3]), acc[i][mt][3]);
+          acc[i][mt][0] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsv[mt].x, part[i][mt][0]), acc[i][mt][0]);
+          acc[i][mt][1] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsv[mt].y, part[i][mt][1]), acc[i][mt][1]);
+          acc[i][mt][2] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsv[mt].x, part[i][mt][2]), acc[i][mt][2]);
+          acc[i][mt][3] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsv[mt].y, part[i][mt][3]), acc[i][mt][3]);
         } else {
           acc[i][mt][0] = fmaf(sc[2 * i], part[i][mt][0], acc[i][mt][0]);
           acc[i][mt][1] = fmaf(sc[2 * i], part[i][mt][1], acc[i][mt][1]);
@@ -456,108 +460,138 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       // block slot bs = kSPB * js + u of stage js goes to warp (kSPB * (s_base + js) + u) % kCW;
       // every slot's owner releases it once, also past the last block (the stage's empty barrier
       // counts kSPB arrivals)
-      for (int bs = (warp - kSPB * s_base) & (kCW - 1); bs < kSPB * nst && ok; bs += kCW) {
-        const int js = bs / kSPB, u = bs % kSPB;
-        const int s = s_base + js;
-        const int slot = s & (rd - 1);
-        if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
-        const int lb = bs;
-        if (lb >= nb) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty(slot));
-          continue;
-        }
-        {
-          LaneWords<BITS> lw[4];
-          read_block<BITS>(lw, ring + (size_t)slot * SB + u * BITS * 512, LO);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty(slot));       // this block's words are in registers
-          const int b = p * a.pb + lb;
-          const uint8_t* xblk = xb + lb * 256;
-          auto load_group = [&](int gq) {
-            cur = gq;
-            const uint8_t* zrow = zs + (gq - gf) * kZsRow;
-            const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
-            const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
+      // The block loop in two compiled forms: during the CTA's first tile the x sums of the
+      // single-group blocks come from the all-ones MMAs and are kept in a table; later tiles read
+      // them (x is the same for every tile) and skip those MMAs.
+      auto run_blocks = [&](auto reuse_tag) {
+        constexpr bool kReuse = decltype(reuse_tag)::value && kFoldZero<T, BITS>;
+        for (int bs = (warp - kSPB * s_base) & (kCW - 1); bs < kSPB * nst && ok; bs += kCW) {
+          const int js = bs / kSPB, u = bs % kSPB;
+          const int s = s_base + js;
+          const int slot = s & (rd - 1);
+          if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
+          const int lb = bs;
+          if (lb >= nb) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(slot));
+            continue;
+          }
+          {
+            LaneWords<BITS> lw[4];
+            read_block<BITS>(lw, ring + (size_t)slot * SB + u * BITS * 512, LO);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(slot));       // this block's words are in registers
+            const int b = p * a.pb + lb;
+            const uint8_t* xblk = xb + lb * 256;
+            auto load_group = [&](int gq) {
+              cur = gq;
+              const uint8_t* zrow = zs + (gq - gf) * kZsRow;
+              const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
+              const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
 #pragma unroll
-            for (int idx = 0; idx < 4; ++idx) {
-              if constexpr (kFoldZero<T, BITS>) {
-                // magic + stored zero + 1 in fp32: one byte permute builds 2^23 + stored (exact),
-                // one add moves it (exact: integers below 2^24)
-                zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - (8388608.0f - kMagicF<T> - 1.0f);
-              } else {
-                zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
-              }
-            }
-            sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
-            sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
-          };
-          auto chunk_mma = [&](const int c, const bool first) {
-            // both 16-k steps of the chunk: one 16-byte load per m-tile (lanes of absent rows read
-            // row 0; their columns of the product are never stored)
-            uint4 xv[MT8];
-#pragma unroll
-            for (int mt = 0; mt < MT8; ++mt) xv[mt] = *reinterpret_cast<const uint4*>(xblk + xoff[mt] + 64 * c);
-#pragma unroll
-            for (int s2 = 0; s2 < 2; ++s2) {
-              const int p0 = 4 * c + 2 * s2;
-#pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                uint32_t af[4];
+              for (int idx = 0; idx < 4; ++idx) {
                 if constexpr (kFoldZero<T, BITS>) {
-                  af[0] = operand_raw<T, BITS>(lw[2 * i], p0);
-                  af[1] = operand_raw<T, BITS>(lw[2 * i + 1], p0);
-                  af[2] = operand_raw<T, BITS>(lw[2 * i], p0 + 1);
-                  af[3] = operand_raw<T, BITS>(lw[2 * i + 1], p0 + 1);
+                  // magic + stored zero + 1 in fp32: one byte permute builds 2^23 + stored (exact),
+                  // one add moves it (exact: integers below 2^24)
+                  zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - (8388608.0f - kMagicF<T> - 1.0f);
                 } else {
-                  af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
-                  af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
-                  af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
-                  af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
+                  zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
                 }
+              }
+              sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
+              sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+            };
+            auto chunk_mma = [&](const int c, const bool first, auto ones_tag) {
+              constexpr bool kOnes = decltype(ones_tag)::value;
+              // both 16-k steps of the chunk: one 16-byte load per m-tile (lanes of absent rows read
+              // row 0; their columns of the product are never stored)
+              uint4 xv[MT8];
+#pragma unroll
+              for (int mt = 0; mt < MT8; ++mt) xv[mt] = *reinterpret_cast<const uint4*>(xblk + xoff[mt] + 64 * c);
+#pragma unroll
+              for (int s2 = 0; s2 < 2; ++s2) {
+                const int p0 = 4 * c + 2 * s2;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  uint32_t af[4];
+                  if constexpr (kFoldZero<T, BITS>) {
+                    af[0] = operand_raw<T, BITS>(lw[2 * i], p0);
+                    af[1] = operand_raw<T, BITS>(lw[2 * i + 1], p0);
+                    af[2] = operand_raw<T, BITS>(lw[2 * i], p0 + 1);
+                    af[3] = operand_raw<T, BITS>(lw[2 * i + 1], p0 + 1);
+                  } else {
+                    af[0] = operand<T, BITS>(lw[2 * i], p0, zq[2 * i]);
+                    af[1] = operand<T, BITS>(lw[2 * i + 1], p0, zq[2 * i + 1]);
+                    af[2] = operand<T, BITS>(lw[2 * i], p0 + 1, zq[2 * i]);
+                    af[3] = operand<T, BITS>(lw[2 * i + 1], p0 + 1, zq[2 * i + 1]);
+                  }
+#pragma unroll
+                  for (int mt = 0; mt < MT8; ++mt) {
+                    if (first && s2 == 0) mma16816_z<T>(part[i][mt], af, xv[mt].x, xv[mt].y);
+                    else mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                  }
+                }
+                if constexpr (kFoldZero<T, BITS> && kOnes) {
+                  const uint32_t ones[4] = {kOnes2<T>, kOnes2<T>, kOnes2<T>, kOnes2<T>};
+#pragma unroll
+                  for (int mt = 0; mt < MT8; ++mt) {
+                    if (first && s2 == 0) mma16816_z<T>(xsp[mt], ones, xv[mt].x, xv[mt].y);
+                    else mma16816<T>(xsp[mt], ones, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                  }
+                }
+              }
+            };
+            // Every block's partial sums are folded into the total at the block's end (per block or
+            // per group change, the sum of scaled partials is the same), so no state crosses blocks.
+            const int g0 = cg[4 * b], g3 = cg[4 * b + 3];
+            if (g0 == g3) {
+              // one group for the whole block (cgid ascends): no branch between the chunks; the first
+              // MMA starts the partial sums from zero
+              if (g0 != cur) load_group(g0);
+              if constexpr (kReuse) {
+                // x sums of this block from the table written during the CTA's first tile
+#pragma unroll
+                for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0, std::false_type{});
+#pragma unroll
+                for (int mt = 0; mt < MT8; ++mt)
+                  xsv[mt] = *reinterpret_cast<const float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0, std::true_type{});
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt) {
-                  if (first && s2 == 0) mma16816_z<T>(part[i][mt], af, xv[mt].x, xv[mt].y);
-                  else mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+                  xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
+                  if (kFoldZero<T, BITS> && g == 0)
+                    *reinterpret_cast<float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t) = xsv[mt];
                 }
               }
-              if constexpr (kFoldZero<T, BITS>) {
-                const uint32_t ones[4] = {kOnes2<T>, kOnes2<T>, kOnes2<T>, kOnes2<T>};
+              flush(false);
+            } else {
+              bool pending = false;
 #pragma unroll
-                for (int mt = 0; mt < MT8; ++mt) {
-                  if (first && s2 == 0) mma16816_z<T>(xsp[mt], ones, xv[mt].x, xv[mt].y);
-                  else mma16816<T>(xsp[mt], ones, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
+              for (int c = 0; c < 4; ++c) {
+                const int gq = cg[4 * b + c];
+                if (gq != cur) {
+                  if (pending) {
+#pragma unroll
+                    for (int mt = 0; mt < MT8; ++mt) xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
+                    flush(false);
+                  }
+                  load_group(gq);
+                  pending = false;
                 }
+                chunk_mma(c, !pending, std::true_type{});
+                pending = true;
               }
-            }
-          };
-          // Every block's partial sums are folded into the total at the block's end (per block or
-          // per group change, the sum of scaled partials is the same), so no state crosses blocks.
-          const int g0 = cg[4 * b], g3 = cg[4 * b + 3];
-          if (g0 == g3) {
-            // one group for the whole block (cgid ascends): no branch between the chunks; the first
-            // MMA starts the partial sums from zero
-            if (g0 != cur) load_group(g0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0);
-            flush(false);
-          } else {
-            bool pending = false;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int gq = cg[4 * b + c];
-              if (gq != cur) {
-                if (pending) flush(false);
-                load_group(gq);
-                pending = false;
-              }
-              chunk_mma(c, !pending);
-              pending = true;
+              for (int mt = 0; mt < MT8; ++mt) xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
+              flush(false);
             }
-            flush(false);
           }
         }
-      }
+      };
+      if (ti > T0) run_blocks(std::true_type{});
+      else run_blocks(std::false_type{});
       s_base += nst;
       __syncwarp();
       if (lane == 0) mbar_arrive(hempty(hs));
@@ -616,7 +650,7 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
-  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_bar, smem, cw;
+  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw;
 };
 
 template <int BITS, int MT8>
@@ -651,7 +685,8 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   const int zs_bytes = 2 * p.span_max * kZsRow;
   const int red_bytes = p.cw * MT8 * 8 * (kTileN + 4) * 4;
   const int cg_bytes = (NB * 4 * 4 + 15) / 16 * 16;
-  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + 4 * 8 + 16;
+  const int xs_bytes = NB * 8 * MT8 * 4;      // x sums per block, reused by every tile after the first
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + 4 * 8 + 16;
   const int SB = stage_bytes<BITS>();
   int budget = target - fixed - 128;
   int rd = budget / (SB + 16);
@@ -668,7 +703,8 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   p.o_zs = p.o_x + (x_bytes + 15) / 16 * 16;
   p.o_red = p.o_zs + zs_bytes;
   p.o_cg = p.o_red + red_bytes;
-  p.o_bar = p.o_cg + cg_bytes;
+  p.o_xs = p.o_cg + cg_bytes;
+  p.o_bar = p.o_xs + xs_bytes;
   p.smem = p.o_bar + (2 * rdp + 4) * 8 + 128;     // + alignment slack of the base
   return p.smem <= 227 * 1024;
 }
@@ -714,7 +750,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   }
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
-                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar};
+                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
