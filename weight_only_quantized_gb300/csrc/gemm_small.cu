@@ -469,8 +469,22 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           const int js = bs / kSPB, u = bs % kSPB;
           const int s = s_base + js;
           const int slot = s & (rd - 1);
-          if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
           const int lb = bs;
+          const int b = p * a.pb + lb;
+          // The block's groups and the zeros and scales of its first group are read before the
+          // wait for its codes: they do not depend on the stage, so their load latency overlaps the
+          // wait and the code loads.
+          int g0 = 0, g3 = 0;
+          uint32_t zw0 = 0;
+          uint2 sw0 = make_uint2(0u, 0u);
+          if (lb < nb) {
+            g0 = cg[4 * b];
+            g3 = cg[4 * b + 3];
+            const uint8_t* zrow = zs + (g0 - gf) * kZsRow;
+            zw0 = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
+            sw0 = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
+          }
+          if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
           if (lb >= nb) {
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(slot));
@@ -481,13 +495,9 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             read_block<BITS>(lw, ring + (size_t)slot * SB + u * BITS * 512, LO);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(slot));       // this block's words are in registers
-            const int b = p * a.pb + lb;
             const uint8_t* xblk = xb + lb * 256;
-            auto load_group = [&](int gq) {
+            auto set_group = [&](const int gq, const uint32_t zw, const uint2 sw) {
               cur = gq;
-              const uint8_t* zrow = zs + (gq - gf) * kZsRow;
-              const uint32_t zw = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
-              const uint2 sw = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
 #pragma unroll
               for (int idx = 0; idx < 4; ++idx) {
                 if constexpr (kFoldZero<T, BITS>) {
@@ -500,6 +510,10 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
               }
               sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
               sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+            };
+            auto load_group = [&](const int gq) {
+              const uint8_t* zrow = zs + (gq - gf) * kZsRow;
+              set_group(gq, *reinterpret_cast<const uint32_t*>(zrow + 4 * g), *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g));
             };
             auto chunk_mma = [&](const int c, const bool first, auto ones_tag) {
               constexpr bool kOnes = decltype(ones_tag)::value;
@@ -543,18 +557,18 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             };
             // Every block's partial sums are folded into the total at the block's end (per block or
             // per group change, the sum of scaled partials is the same), so no state crosses blocks.
-            const int g0 = cg[4 * b], g3 = cg[4 * b + 3];
             if (g0 == g3) {
               // one group for the whole block (cgid ascends): no branch between the chunks; the first
               // MMA starts the partial sums from zero
-              if (g0 != cur) load_group(g0);
+              if (g0 != cur) set_group(g0, zw0, sw0);
               if constexpr (kReuse) {
-                // x sums of this block from the table written during the CTA's first tile
-#pragma unroll
-                for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0, std::false_type{});
+                // x sums of this block from the table written during the CTA's first tile (read
+                // before the MMAs, so that the load is off the way to the flush)
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt)
                   xsv[mt] = *reinterpret_cast<const float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0, std::false_type{});
               } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) chunk_mma(c, c == 0, std::true_type{});
