@@ -2,7 +2,7 @@
 
 The path is forced with gptq_gemm_path so it is checked at small M too.  Shapes cover every bit
 width, both dtypes, act-order (x gathered into the workspace), padded K, ragged N and M tails
-that leave part of a 128-row tile empty.
+that leave part of an x tile (64, 128 or 256 rows, chosen by M) empty.
 """
 import numpy as np
 import pytest
@@ -34,11 +34,11 @@ def _id(s):
 
 
 @pytest.mark.parametrize("spec", SPECS, ids=_id)
-@pytest.mark.parametrize("M", [1, 17, 128, 200])
+@pytest.mark.parametrize("M", [1, 17, 64, 65, 128, 129, 200, 300])
 def test_large_path_parity(spec, M):
     ck = synth.make_checkpoint(spec, seed=spec.K + spec.N + spec.bits)
     h = repack(ck)
-    gptq.gptq_reserve(h, 256)
+    gptq.gptq_reserve(h, 300)
     x = synth.make_x(M, spec.K, spec.dtype, seed=M + 7)
     compare(run_gemm(h, x, spec.N, gptq.PATH_LARGE_M), oracle_y(ck, x))
     gptq.gptq_device_status(h)

@@ -12,8 +12,9 @@
 // and the group scale multiplies that partial sum in fp32 -- the same arithmetic as the small-M
 // kernel, inside the k reduction.
 //
-// Design on sm_103a, one CTA per tile of 128 output features x 256 rows of x (swap-AB: D[n][m]):
-//  * warp 0: x producer, TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of 256 x 64 x tiles;
+// Design on sm_103a, one CTA per tile of 128 output features x BMX rows of x (swap-AB: D[n][m];
+// BMX = 64, 128 or 256, the smallest that covers M, so a mid-size M does not pay for 256 rows):
+//  * warp 0: x producer, TMA (cp.async.bulk.tensor.2d, SWIZZLE_128B) loads of BMX x 64 x tiles;
 //    warp 2: code producer, cp.async.bulk copies of each packed 128-row block of the tile's 128
 //    columns plus the stored zeros of its four chunks; each into a ring tracked by mbarriers.
 //  * warps 4..7: dequantisers, one per SM sub-partition.  Thread d owns weight row n0 + d: one LOP3
@@ -21,11 +22,11 @@
 //    integer code - zero, and the row is written in the UMMA K-major SWIZZLE_128B layout (16-byte
 //    chunk j of row r at chunk j ^ (r % 8) of its 128-byte row), then a generic-to-async proxy
 //    fence and an arrive.
-//  * warp 1: allocates all 512 TMEM columns (two 256-column partial-sum buffers); the warp runs
+//  * warp 1: allocates all 512 TMEM columns (512 / BMX partial-sum buffers of BMX columns); the warp runs
 //    the schedule and one elected lane issues tcgen05.mma.cta_group::1.kind::f16 (M = 128 weight
-//    rows, N = 256 x rows, K = 16), two per 32-row chunk, restarting the accumulator at each group
+//    rows, N = BMX x rows, K = 16), two per 32-row chunk, restarting the accumulator at each group
 //    and committing the buffer when the group ends.
-//  * warps 8..15: eight scaler warps, two per TMEM lane quarter, 128 columns each.  Per group:
+//  * warps 8..15: eight scaler warps, two per TMEM lane quarter, BMX / 2 columns each.  Per group:
 //    tcgen05.ld the partial sums (16 columns in flight while the previous 16 are used),
 //    S += scale[g][n] * P in registers, release the buffer.  At the end they round S to the output
 //    type and store y.  setmaxnreg gives them 184 registers a thread and the other warps 72.
@@ -39,25 +40,35 @@
 namespace gptq {
 namespace {
 
-constexpr int BN = 128, BMX = 256, HK = 64;   // weight rows (MMA M), x rows (MMA N), k per stage
+constexpr int BN = 128, HK = 64;   // weight rows (MMA M), k per stage; x rows per tile (MMA N): BMX
 // Four warpgroups: {x producer, MMA issuer, code producer, spare}, four dequantisers (one per SM sub-partition),
-// and eight scalers (two per TMEM lane quarter, 128 fp32 sums a thread).  setmaxnreg moves
+// and eight scalers (two per TMEM lane quarter, BMX / 2 fp32 sums a thread).  setmaxnreg moves
 // registers from the first two warpgroups to the scalers: 2 x 128 x (72 + 184) = 65536.
 constexpr int kDqWarps = 4, kScWarps = 8;
 constexpr int kDqWarp0 = 4, kScWarp0 = 8;
 constexpr int kThreadsL = 512;
 constexpr int kRegsLaunch = 128, kRegsLight = 72, kRegsScaler = 184;
 static_assert(2 * 128 * (kRegsLight + kRegsScaler) <= kThreadsL * kRegsLaunch, "register split exceeds the launch");
-constexpr int XS = 3, WS = 3;
-constexpr int X_BYTES = BMX * HK * 2;           // 32 KB
+// Ring depths.  A weight stage passes dequantisers -> proxy fence -> MMA issue -> tcgen05 commit
+// before it is free again, a round trip of a few thousand cycles; with a small x tile the MMA
+// of a stage is short, so the weight ring must be deeper to keep that round trip off the critical
+// path.  x stages are small then, and four cover the TMA load latency.
+template <int BITS, int BMX> constexpr int XS = BMX <= 128 ? 4 : (BITS == 8 ? 3 : 4);
+template <int BMX> constexpr int WS = BMX == 256 ? 3 : 4;
+template <int BMX> constexpr int X_BYTES = BMX * HK * 2;   // 32 KB at BMX = 256
 constexpr int W_BYTES = BN * HK * 2;            // 16 KB
-constexpr int kTmemCols = 512;                  // two partial-sum buffers of 256 columns
+// Partial-sum buffers in tensor memory: all 512 columns, BMX each.  The MMA can run NPB - 1 groups
+// ahead of the scalers, so the commit -> scaler -> release round trip of one buffer is hidden
+// behind the other buffers when the x tile is narrow.
+template <int BMX> constexpr int NPB = 512 / BMX;          // 8, 4 or 2
+constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 template <int BITS> constexpr int PK_BYTES = BN * 16 * BITS;  // one 128-row block of 128 columns
 // A packed stage: the block's codes, then the stored zero of each of its four 32-row chunks for the
 // tile's 128 columns (copied by the producer, so the dequant warps never wait on global loads).
 template <int BITS> constexpr int PKS_BYTES = PK_BYTES<BITS> + 4 * BN;
-template <int BITS> constexpr int PSB = BITS == 8 ? 3 : 4;     // packed stages in the ring
+// packed stages in the code ring: the bytes in flight per SM must cover the HBM latency
+template <int BITS, int BMX> constexpr int PSB = BMX == 256 ? (BITS == 8 ? 3 : 4) : (BITS == 8 ? 4 : 8);
 
 template <typename T> struct MagicL;
 template <> struct MagicL<__half> { static constexpr uint32_t bits = 0x6400u; };
@@ -65,12 +76,12 @@ template <> struct MagicL<__nv_bfloat16> { static constexpr uint32_t bits = 0x43
 template <typename T, int BITS> constexpr bool kF32Path = BITS == 8 && std::is_same<T, __nv_bfloat16>::value;
 
 // Shared-memory carve-up from a 1024-byte-aligned base.
-template <int BITS> struct LargeSmem {
+template <int BITS, int BMX> struct LargeSmem {
   static constexpr int x = 0;
-  static constexpr int w = x + XS * X_BYTES;
-  static constexpr int pk = w + WS * W_BYTES;
-  static constexpr int bars = pk + PSB<BITS> * PKS_BYTES<BITS>;
-  static constexpr int nbars = 2 * XS + 2 * WS + 2 * PSB<BITS> + 5;
+  static constexpr int w = x + XS<BITS, BMX> * X_BYTES<BMX>;
+  static constexpr int pk = w + WS<BMX> * W_BYTES;
+  static constexpr int bars = pk + PSB<BITS, BMX> * PKS_BYTES<BITS>;
+  static constexpr int nbars = 2 * XS<BITS, BMX> + 2 * WS<BMX> + 2 * PSB<BITS, BMX> + 2 * NPB<BMX> + 1;
   static constexpr int tmem_slot = bars + nbars * 8;
   static constexpr int cg = tmem_slot + 16;       // int32 group of every 32-row chunk, then one
                                                   // uint32 group-end mask per 32 chunks
@@ -205,17 +216,36 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                : "r"(addr));
 }
+// Wait for every tcgen05.ld of this thread; the registers of the loads are named by the
+// reg_after_wait calls that follow, so no use of them is scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_all() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void reg_after_wait(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :: "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                :: "memory");
 }
-template <typename T, int BITS>
+template <typename T, int BITS, int BMX>
 __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, const __grid_constant__ CUtensorMap tmap_x) {
-  using S = LargeSmem<BITS>;
+  static_assert(BMX == 64 || BMX == 128 || BMX == 256, "MMA N: a multiple of 16 up to 256; TMEM: a power of two");
+  using S = LargeSmem<BITS, BMX>;
+  constexpr int XB = X_BYTES<BMX>;
+  constexpr int XS = gptq::XS<BITS, BMX>;
+  constexpr int WS = gptq::WS<BMX>;
+  constexpr int kCols = kTmemCols;
+  constexpr int NP_ = NPB<BMX>;
+  constexpr int kDq = kDqWarps, kSc = kScWarps, kSc0 = kScWarp0;
+  constexpr int HC = BMX / 2;                 // x rows (TMEM columns) per scaler warp
   constexpr int PKB = PKS_BYTES<BITS>;
-  constexpr int PS = PSB<BITS>;
+  constexpr int PS = PSB<BITS, BMX>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -236,26 +266,24 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   auto pk_full = [&](int i) { return bar + 8 * (2 * XS + 2 * WS + i); };
   auto pk_empty = [&](int i) { return bar + 8 * (2 * XS + 2 * WS + PS + i); };
   auto p_full = [&](int b) { return bar + 8 * (2 * XS + 2 * WS + 2 * PS + b); };
-  auto p_empty = [&](int b) { return bar + 8 * (2 * XS + 2 * WS + 2 * PS + 2 + b); };
-  const uint32_t mma_done = bar + 8 * (2 * XS + 2 * WS + 2 * PS + 4);
+  auto p_empty = [&](int b) { return bar + 8 * (2 * XS + 2 * WS + 2 * PS + NP_ + b); };
+  const uint32_t mma_done = bar + 8 * (2 * XS + 2 * WS + 2 * PS + 2 * NP_);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + S::tmem_slot);
   int32_t* cg = reinterpret_cast<int32_t*>(base + S::cg);
   uint32_t* gmask = reinterpret_cast<uint32_t*>(base + S::cg + 4 * nchunks);
   const int nwin = (nchunks + 31) / 32;
-  // a 32-row chunk c ends its group when the next chunk has another group (or c is the last)
-  auto group_ends = [&](int c) { return c + 1 == nchunks || cg[c + 1] != cg[c]; };
 
   if (tid == 0) {
     for (int i = 0; i < XS; ++i) { mbar_init(x_full(i), 1); mbar_init(x_empty(i), 1); }
-    for (int i = 0; i < WS; ++i) { mbar_init(w_full(i), kDqWarps); mbar_init(w_empty(i), 1); }
-    for (int i = 0; i < PS; ++i) { mbar_init(pk_full(i), 1); mbar_init(pk_empty(i), kDqWarps); }
-    for (int b = 0; b < 2; ++b) { mbar_init(p_full(b), 1); mbar_init(p_empty(b), kScWarps); }
+    for (int i = 0; i < WS; ++i) { mbar_init(w_full(i), kDq); mbar_init(w_empty(i), 1); }
+    for (int i = 0; i < PS; ++i) { mbar_init(pk_full(i), 1); mbar_init(pk_empty(i), kDq); }
+    for (int b = 0; b < NP_; ++b) { mbar_init(p_full(b), 1); mbar_init(p_empty(b), kSc); }
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
+                 :: "r"(smem_u32(tmem_slot)), "r"(kCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   for (int i = tid; i < nchunks; i += kThreadsL) cg[i] = __ldg(&a.cgid[i]);
@@ -273,56 +301,105 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   bool ok = true;
-  if (warp >= kScWarp0) {
+  if (warp >= kSc0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsScaler));
     // ---------------- scalers: S += scale * P per group, then y ----------------
-    const int sw = warp - kScWarp0;
+    const int sw = warp - kSc0;
     const int q = warp & 3;                   // TMEM lane quarter this warp may access
-    const int hs = sw >> 2;                   // 128-column half of the 256 x rows
+    const int hs = sw >> 2;                   // half of the BMX x rows
     const int nrow = 32 * q + lane;           // weight row of this thread inside the tile
     const int n = n0 + nrow;
-    float acc[128];
+    float acc[HC];
 #pragma unroll
-    for (int j = 0; j < 128; ++j) acc[j] = 0.f;
-    int gi = 0;
-    float sc_next = 0.f;
-    // the scale of the group that starts at chunk c
-    auto scale_at = [&](int c) { return scale_f<T>(__ldg(&a.s_r[(size_t)cg[c] * a.Np + n])); };
-    if (nchunks > 0) sc_next = scale_at(0);
-    for (int c = 0; c < nchunks && ok; ++c) {
-      if (!group_ends(c)) continue;
-      const float sc = sc_next;
-      if (c + 1 < nchunks) sc_next = scale_at(c + 1);     // next group's scale, ahead of use
-      const int b = gi & 1;
-      if (!mbar_wait(p_full(b), (gi >> 1) & 1)) { ok = false; break; }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * 256 + 128 * hs);
-      uint32_t ra[16], rb[16];
-      tmem_ld16(taddr, ra);
-      tmem_wait_ld(ra);
-#pragma unroll
-      for (int part = 0; part < 8; part += 2) {
-        tmem_ld16(taddr + 16 * (part + 1), rb);             // next 16 columns in flight while ra is used
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[16 * part + j] = fmaf(sc, __uint_as_float(ra[j]), acc[16 * part + j]);
-        tmem_wait_ld(rb);
-        if (part + 2 < 8) tmem_ld16(taddr + 16 * (part + 2), ra);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[16 * (part + 1) + j] = fmaf(sc, __uint_as_float(rb[j]), acc[16 * (part + 1) + j]);
-        if (part + 2 < 8) tmem_wait_ld(ra);
+    for (int j = 0; j < HC; ++j) acc[j] = 0.f;
+    // Scales of the next kSq groups in flight: each CTA reads its own columns' scales once, from
+    // HBM, so a load issued only one group ahead left every group waiting for it.  The groups are
+    // visited in order of their last chunk, walking the group-end mask.
+    constexpr int kSq = 8;
+    int ew = 0;                               // mask word of the next group end not yet prefetched
+    uint32_t ebits = nwin > 0 ? gmask[0] : 0u;
+    auto next_end = [&]() -> int {            // chunk that ends the next group, -1 after the last
+      while (ebits == 0u) {
+        if (++ew >= nwin) return -1;
+        ebits = gmask[ew];
       }
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_empty(b));
-      ++gi;
+      const int j = __ffs(ebits) - 1;
+      ebits &= ebits - 1u;
+      return 32 * ew + j;
+    };
+    auto scale_of_end = [&](int e) { return e >= 0 ? scale_f<T>(__ldg(&a.s_r[(size_t)cg[e] * a.Np + n])) : 0.f; };
+    int ng = 0;                               // groups in K
+    for (int w = 0; w < nwin; ++w) ng += __popc(gmask[w]);
+    float sq[kSq];
+#pragma unroll
+    for (int j = 0; j < kSq; ++j) sq[j] = scale_of_end(next_end());
+    // GB groups per pass: their buffers are waited for, all their columns loaded back to back and
+    // waited for once, then released together (one tcgen05.ld round trip per pass, not per group;
+    // the MMA runs NP_ groups ahead, so it still has GB buffers to fill meanwhile)
+    // (BMX = 64: four groups of 32 columns, 128 registers of loads; wider tiles: one group, 64
+    // columns per round, as the accumulators themselves take 64 or 128 registers)
+    constexpr int GB = BMX == 64 ? 4 : 1;
+    constexpr int RC = BMX == 64 ? HC : 64;          // columns of one group per load round
+    static_assert(kSq % GB == 0 && NP_ >= 2 * GB, "scaler batching");
+    for (int g0 = 0; g0 < ng && ok; g0 += kSq) {
+#pragma unroll
+      for (int jb = 0; jb < kSq; jb += GB) {
+        const int gb0 = g0 + jb;
+        if (gb0 >= ng || !ok) break;
+#pragma unroll
+        for (int j = 0; j < GB; ++j) {
+          const int gi = gb0 + j;
+          if (gi < ng && ok && !mbar_wait(p_full(gi & (NP_ - 1)), (gi / NP_) & 1)) ok = false;
+        }
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int r0 = 0; r0 < HC; r0 += RC) {
+          uint32_t rv[GB][RC / 16][16];
+#pragma unroll
+          for (int j = 0; j < GB; ++j) {
+            const int b = (gb0 + j) & (NP_ - 1);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * BMX + HC * hs + r0);
+            if (gb0 + j < ng)
+#pragma unroll
+              for (int k = 0; k < RC / 16; ++k) tmem_ld16(taddr + 16 * k, rv[j][k]);
+          }
+          tmem_wait_all();
+#pragma unroll
+          for (int j = 0; j < GB; ++j)
+#pragma unroll
+            for (int k = 0; k < RC / 16; ++k) reg_after_wait(rv[j][k]);
+#pragma unroll
+          for (int j = 0; j < GB; ++j) {
+            if (gb0 + j < ng) {
+              const float sc = sq[jb + j];
+#pragma unroll
+              for (int k = 0; k < RC / 16; ++k)
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                  acc[r0 + 16 * k + jj] = fmaf(sc, __uint_as_float(rv[j][k][jj]), acc[r0 + 16 * k + jj]);
+            }
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < GB; ++j) {
+          const int gi = gb0 + j;
+          if (gi < ng) {
+            if (lane == 0) mbar_arrive(p_empty(gi & (NP_ - 1)));
+            sq[jb + j] = scale_of_end(next_end());      // group gi + kSq
+          }
+        }
+      }
     }
     if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-    // y[m][n] for the 128 x rows of this half: lanes are consecutive n, so each store is 64 bytes
+    // y[m][n] for the HC x rows of this half: lanes are consecutive n, so each store is 64 bytes
     uint16_t* y = static_cast<uint16_t*>(a.y);
     if (n < a.N) {
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        const int m = m0 + 128 * hs + j;
+      for (int j = 0; j < HC; ++j) {
+        const int m = m0 + HC * hs + j;
         if (m < a.M) y[(size_t)m * a.N + n] = to_bits<T>(acc[j]);
       }
     }
@@ -336,8 +413,8 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         for (int i = 0; i < nhalf && ok; ++i) {
           const int xs = i % XS;
           if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(x_full(xs), X_BYTES);
-          tma_load_2d(xs_s + xs * X_BYTES, &tmap_x, i * HK, m0, x_full(xs));
+          mbar_arrive_expect_tx(x_full(xs), XB);
+          tma_load_2d(xs_s + xs * XB, &tmap_x, i * HK, m0, x_full(xs));
           ++x_issued;
         }
         // every issued copy must land before the CTA may exit
@@ -392,7 +469,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
           mbar_wait_poison(w_full(ws), wph, limit);
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint64_t ad = smem_desc_sw128(ws_s + ws * W_BYTES);     // A: weights, 128 rows
-          const uint64_t bd = smem_desc_sw128(xs_s + xs * X_BYTES);     // B: x, 256 rows
+          const uint64_t bd = smem_desc_sw128(xs_s + xs * XB);          // B: x, BMX rows
   #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * i + cc;
@@ -400,12 +477,12 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
               cur = nxt;
               nxt = (c >> 5) + 1 < nwin ? gmask[(c >> 5) + 1] : 0u;
             }
-            const int b = gi & 1;
-            if (fresh && gi >= 2) {
-              mbar_wait_poison(p_empty(b), ((gi >> 1) - 1) & 1, limit);
+            const int b = gi & (NP_ - 1);
+            if (fresh && gi >= NP_) {
+              mbar_wait_poison(p_empty(b), ((gi / NP_) - 1) & 1, limit);
               asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             }
-            const uint32_t d = tmem + (uint32_t)(b * 256);
+            const uint32_t d = tmem + (uint32_t)(b * BMX);
             umma_f16_if(d, ad + 4 * cc, bd + 4 * cc, idesc, fresh ^ 1u, me);
             umma_f16_if(d, ad + 4 * cc + 2, bd + 4 * cc + 2, idesc, 1u, me);
             const uint32_t end = (cur >> (c & 31)) & 1u;
@@ -423,7 +500,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         mbar_wait_poison(mma_done, 0, limit);
         if (limit == 0 && me) atomicExch(a.err, DEV_ERR_TIMEOUT);
       }
-    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+    } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDq) {
       // ---------------- dequantisers: thread owns weight row n0 + nrow ----------------
       const int nrow = 32 * (warp - kDqWarp0) + lane;
       uint32_t zq[4];
@@ -469,7 +546,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kCols) : "memory");
   }
 }
 
@@ -483,20 +560,24 @@ __global__ void k_permute_x(const uint16_t* __restrict__ x, const int32_t* __res
     }
 }
 
-template <int BITS> size_t large_smem_bytes(int Kr) {
-  return 1024 + LargeSmem<BITS>::cg + (size_t)(Kr / 32) * 4 + (size_t)((Kr / 32 + 31) / 32) * 4;
+template <int BITS, int BMX> size_t large_smem_bytes(int Kr) {
+  return 1024 + LargeSmem<BITS, BMX>::cg + (size_t)(Kr / 32) * 4 + (size_t)((Kr / 32 + 31) / 32) * 4;
 }
 
-template <typename T, int BITS>
-cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
-  const size_t smem = large_smem_bytes<BITS>(h.Kr);
-  auto kern = k_gemm_large<T, BITS>;
+// x rows per tile: the smallest of 64, 128, 256 that covers M (and 256 above it)
+inline int bmx_for(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+
+template <typename T, int BITS, int BMX>
+cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
+  const size_t smem = large_smem_bytes<BITS, BMX>(h.Kr);
+  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+  auto kern = k_gemm_large<T, BITS, BMX>;
   // setmaxnreg redistributes the registers the block is launched with; a launch with fewer than
   // kRegsLaunch a thread could never satisfy the scalers' increase, so refuse it.
   static const int regs = [&] {
     cudaFuncAttributes fa;
     return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : -1;
-  }();
+  }();   // one per instantiation
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -512,6 +593,15 @@ cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, c
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args, map);
+}
+
+template <typename T, int BITS>
+cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
+  switch (bmx_for(M)) {
+    case 64: return launch_tbm<T, BITS, 64>(h, map, y, M, st);
+    case 128: return launch_tbm<T, BITS, 128>(h, map, y, M, st);
+    default: return launch_tbm<T, BITS, 256>(h, map, y, M, st);
+  }
 }
 
 template <typename T>
@@ -543,7 +633,7 @@ bool large_m_available() { return true; }
 int large_m_launches(const Handle& h, int M) { return M > 0 ? (h.identity ? 1 : 2) : 0; }
 
 cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  if (large_smem_bytes<8>(h.Kr) > 227 * 1024) return cudaErrorInvalidConfiguration;
+  if (large_smem_bytes<8, 256>(h.Kr) > 227 * 1024) return cudaErrorInvalidConfiguration;
   const void* src = x;
   int kdim = h.K;
   if (!h.identity) {
@@ -559,7 +649,7 @@ cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cu
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)kdim, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)kdim * 2};
-  const cuuint32_t box[2] = {HK, BMX};
+  const cuuint32_t box[2] = {HK, (cuuint32_t)bmx_for(M)};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = h.dtype == GPTQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (enc(&map, dt, 2, const_cast<void*>(src), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
