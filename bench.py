@@ -390,8 +390,49 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
     one("llama3-70b-gate-8192x28672-b4g128-descact", s3, m3, 4)
     s4, m4 = synth.workload("prefill-8192x28672-b4g128")
     one("prefill-8192x28672-b4g128", s4, [4096] if args.quick_prefill else m4, 1)
+    if not args.no_sweep:
+        out["format-sweep-4096x4096"] = format_sweep(hbm, tf_burst)
     out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "kind": peak_kind}
     return out
+
+
+def format_sweep(hbm, tf_burst):
+    """K = N = 4096 at bits 2/3/8 (group 128) and bits 4 at groups -1/32/64, M = 1/32/256.
+
+    One seeded checkpoint per format, repacked into as many handles as it takes for the rotated
+    weights to cover three L2 sizes, so every call streams its weights from HBM."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    res = {}
+    for spec in synth.format_sweep():
+        name = f"b{spec.bits}g{spec.group_size}{'-descact' if spec.desc_act else ''}"
+        B1 = b_alg(spec, 1)
+        nl = max(4, min(128, -(-3 * l2 // B1)))
+        ck = synth.make_checkpoint(spec, seed=7)
+        dev = [t.cuda() if t is not None else None for t in (ck.qweight, ck.qzeros, ck.scales, ck.g_idx)]
+        hs = [gptq.gptq_repack(dev[0], dev[1], dev[2], dev[3], spec.bits, spec.group_size) for _ in range(nl)]
+        for h in hs:
+            gptq.gptq_reserve(h, max(synth.SWEEP_M))
+        torch.cuda.synchronize()
+        r = {"layers_rotated": nl}
+        for M in synth.SWEEP_M:
+            xs = [synth.make_x(M, spec.K, spec.dtype, seed=M + i).cuda() for i in range(4)]
+            ys = [torch.empty(M, spec.N, dtype=torch.float16, device="cuda") for _ in range(4)]
+            n = 200 if M <= 64 else 50
+            t = time_calls(hs, xs, ys, M, n, 3, graph=True)
+            B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
+            roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
+            r[f"M={M}"] = {"us": round(t * 1e6, 2), "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),
+                           "roofline_frac": round(roof / t, 4),
+                           "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+            del xs, ys
+        for h in hs:
+            h.close()
+        del hs, dev
+        torch.cuda.empty_cache()
+        res[name] = r
+    return res
 
 
 PROFILE_LAYERS = {"decode": WORKLOAD, "gate": "llama3-70b-gate-8192x28672-b4g128-descact",
@@ -426,6 +467,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-extra", action="store_true", help="skip the other layers and M values")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the K = N = 4096 format sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--quick-prefill", action="store_true", help="prefill at M=4096 only")
