@@ -71,3 +71,5 @@ def test_auto_dispatch_uses_large_path_above_16():
     spec = synth.LayerSpec(256, 256, 4, 128, True)
     h = repack(synth.make_checkpoint(spec))
     assert gptq.gptq_gemm_launches(h, 64) == 2          # gather pre-pass + tcgen05 kernel
+    assert gptq.gptq_gemm_launches(h, 1) == 1           # small-M kernel gathers x itself at M <= 2
+    assert gptq.gptq_gemm_launches(h, 5) == 2           # pre-pass above that

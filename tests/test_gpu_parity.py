@@ -49,7 +49,7 @@ def test_repack_bit_exact(spec):
 
 
 @pytest.mark.parametrize("spec", SPECS, ids=_id)
-@pytest.mark.parametrize("M", [1, 5, 8, 16, 17, 40])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 16, 17, 40])
 def test_gemm_parity_small_layers(spec, M):
     ck = synth.make_checkpoint(spec, seed=spec.N + spec.bits)
     h = repack(ck)

@@ -268,6 +268,12 @@ struct SmallArgs {
   int x_row;        // bytes of one staged x row: pb * 256 + 64 (rows 64 bytes apart mod 128)
   int o_x, o_zs, o_red, o_cg, o_bar;   // shared-memory offsets; the ring starts at 0
   int o_xs;         // x sums of the single-group blocks [NB][8 MT8] (fp32)
+  // act-order with x staged once and M <= 2: the producer copies the caller's x rows and perm
+  // into shared memory and the consumers permute x there (no pre-pass launch)
+  const int32_t* perm;
+  int gather;
+  int o_pm;         // int32 [Kr] copy of perm (-1: pad row)
+  int o_raw;        // the caller's x rows, [M][K] as given
 };
 
 template <int CW>
@@ -275,7 +281,7 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
 }
 
-template <typename T, int BITS, int MT8, int CW>
+template <typename T, int BITS, int MT8, int CW, bool GATHER>
 __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
   constexpr int kCW = CW;
   constexpr int kThreadsS = threads_of<CW>();
@@ -302,6 +308,8 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   auto empty = [&](int i) { return bar0 + 8u * (rd + i); };
   auto hfull = [&](int i) { return bar0 + 8u * (2 * rd + i); };
   auto hempty = [&](int i) { return bar0 + 8u * (2 * rd + 2 + i); };
+  const int32_t* pm = reinterpret_cast<const int32_t*>(smem + a.o_pm);
+  uint8_t* rawx = smem + a.o_raw;
   const int zs_bytes = a.span_max * kZsRow;
   const int x_bytes = a.M * a.x_row;
 
@@ -330,6 +338,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     int s_issued = 0;               // weight stages issued
     int q = 0;                      // segments (tile, panel) started
     int s_sent = 0, q_sent = 0;     // stages and segment headers actually issued
+
     for (int ti = T0; ti < T1; ++ti) {
       for (int p = 0; p < a.npanel; ++p, ++q) {
         const int nb = panel_blocks(p);
@@ -339,10 +348,14 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
         const int gf = cg[4 * p * a.pb], gl = cg[4 * (p * a.pb + nb) - 1];
         const bool load_x = !a.single || q == 0;
         const uint32_t zs_tx = (uint32_t)(gl - gf + 1) * kZsRow;
-        const uint32_t x_tx = load_x ? (uint32_t)a.M * nb * 256u : 0u;
+        // x bytes: the staged rows, or (gathering) perm and the caller's rows as given
+        const uint32_t x_tx = !load_x ? 0u : GATHER ? (uint32_t)a.Kr * 4u + (uint32_t)a.M * a.ldx * 2u
+                                                    : (uint32_t)a.M * nb * 256u;
         if (go) {
           mbar_arrive_expect_tx(hfull(hs), zs_tx + x_tx);
           bulk_g2s(smem_u32(zsreg + hs * zs_bytes), a.zst + ((size_t)ti * a.G + gf) * kZsRow, zs_tx, hfull(hs));
+          if (GATHER && load_x)     // handle data, before the wait on the previous grid
+            bulk_g2s(smem_u32(pm), a.perm, (uint32_t)a.Kr * 4u, hfull(hs));
         }
         q_sent += go ? 1 : 0;
         // weights of the first segment (up to 4 stages) go out before x; x waits for the previous grid
@@ -368,10 +381,15 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           for (; j < pre; ++j) issue_stage(j);
           if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
           if (go) {
-            uint8_t* xd = xreg + (a.single ? 0 : hs * x_bytes);
-            for (int m = 0; m < a.M; ++m)
-              bulk_g2s(smem_u32(xd + m * a.x_row), a.x + (size_t)m * a.ldx + (size_t)p * a.pb * 128,
-                       (uint32_t)nb * 256u, hfull(hs));
+            if constexpr (GATHER) {
+              for (int m = 0; m < a.M; ++m)
+                bulk_g2s(smem_u32(rawx + (size_t)m * a.ldx * 2), a.x + (size_t)m * a.ldx, (uint32_t)a.ldx * 2u, hfull(hs));
+            } else {
+              uint8_t* xd = xreg + (a.single ? 0 : hs * x_bytes);
+              for (int m = 0; m < a.M; ++m)
+                bulk_g2s(smem_u32(xd + m * a.x_row), a.x + (size_t)m * a.ldx + (size_t)p * a.pb * 128,
+                         (uint32_t)nb * 256u, hfull(hs));
+            }
           }
         }
         for (; j < nst; ++j) issue_stage(j);
@@ -452,6 +470,20 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       const int nb = panel_blocks(p);
       const int hs = q & 1;
       if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1))) ok = false;
+      if (GATHER && q == 0) {
+        // x[m][perm[j]] from the copied rows into the staged rows, two sorted rows per store
+        const int half = a.Kr / 2;
+        const uint16_t* rx = reinterpret_cast<const uint16_t*>(rawx);
+        for (int i = tid; i < half; i += kCW * 32) {
+          const int k0 = pm[2 * i], k1 = pm[2 * i + 1];
+          for (int m = 0; m < a.M; ++m) {
+            const uint32_t lo = k0 >= 0 ? rx[(size_t)m * a.ldx + k0] : 0u;
+            const uint32_t hi = k1 >= 0 ? rx[(size_t)m * a.ldx + k1] : 0u;
+            *reinterpret_cast<uint32_t*>(xreg + m * a.x_row + 4 * i) = lo | (hi << 16);
+          }
+        }
+        named_sync_consumers<kCW>();      // every consumer's share of x is in place
+      }
       const uint8_t* xb = xreg + (a.single ? 0 : hs * x_bytes);
       const uint8_t* zs = zsreg + hs * zs_bytes;
       const int gf = cg[4 * p * a.pb];
@@ -664,11 +696,12 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
-  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw;
+  int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw,
+      gather, o_pm, o_raw;
 };
 
-template <int BITS, int MT8>
-bool make_plan(const Handle& h, int M, SmallPlan& p) {
+// Layout for codes of `bits` bits and MT8 m-tiles; with_gather adds the perm copy.
+bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p) {
   const int NB = h.Kr / 128;
   p.ntiles = (h.N + kTileN - 1) / kTileN;
   p.grid = std::min(p.ntiles, h.sm_count);
@@ -679,7 +712,7 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   // call's CTA can start streaming beside it; a long one takes the whole SM, a deeper ring and
   // (at M <= 8) 16 consumer warps.
   const bool short_cta = x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3;
-  p.cw = (MT8 == 1 && !short_cta) ? 16 : 8;
+  p.cw = (mt8 == 1 && !short_cta) ? 16 : 8;
   if (x_all <= kXSingle) {
     p.single = 1;
     p.pb = NB;
@@ -688,6 +721,7 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
     p.single = 0;
     p.pb = std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB);
   }
+  p.gather = (with_gather && p.single) ? 1 : 0;
   p.npanel = (NB + p.pb - 1) / p.pb;
   p.span_max = 1;
   for (int q = 0; q < p.npanel; ++q) {
@@ -697,11 +731,13 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   p.x_row = p.pb * 256 + 64;
   const int x_bytes = (p.single ? 1 : 2) * M * p.x_row;
   const int zs_bytes = 2 * p.span_max * kZsRow;
-  const int red_bytes = p.cw * MT8 * 8 * (kTileN + 4) * 4;
+  const int red_bytes = p.cw * mt8 * 8 * (kTileN + 4) * 4;
   const int cg_bytes = (NB * 4 * 4 + 15) / 16 * 16;
-  const int xs_bytes = NB * 8 * MT8 * 4;      // x sums per block, reused by every tile after the first
-  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + 4 * 8 + 16;
-  const int SB = stage_bytes<BITS>();
+  const int xs_bytes = NB * 8 * mt8 * 4;      // x sums per block, reused by every tile after the first
+  const int pm_bytes = p.gather ? h.Kr * 4 : 0;
+  const int raw_bytes = p.gather ? M * h.K * 2 : 0;
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + 4 * 8 + 16;
+  const int SB = kSPB * bits * 512;
   int budget = target - fixed - 128;
   int rd = budget / (SB + 16);
   if (rd < 4) {   // large tables: take up to a whole SM's shared memory
@@ -718,9 +754,19 @@ bool make_plan(const Handle& h, int M, SmallPlan& p) {
   p.o_red = p.o_zs + zs_bytes;
   p.o_cg = p.o_red + red_bytes;
   p.o_xs = p.o_cg + cg_bytes;
-  p.o_bar = p.o_xs + xs_bytes;
+  p.o_pm = p.o_xs + xs_bytes;
+  p.o_raw = p.o_pm + pm_bytes;
+  p.o_bar = p.o_raw + raw_bytes;
   p.smem = p.o_bar + (2 * rdp + 4) * 8 + 128;     // + alignment slack of the base
   return p.smem <= 227 * 1024;
+}
+
+// The plan: act-order handles gather x in the GEMM kernel at M <= 2 when x is staged once and the
+// weight ring keeps at least eight stages; otherwise a pre-pass gathers x into the workspace.
+bool make_plan(const Handle& h, int M, SmallPlan& p) {
+  const int mt8 = M <= 8 ? 1 : 2;
+  if (!h.identity && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
+  return plan_layout(h, M, h.bits, mt8, false, p);
 }
 
 template <typename T, int BITS, int MT8>
@@ -731,10 +777,13 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
     const int64_t key = ((int64_t)GPTQ_PATH_SMALL_M << 32) | (uint32_t)M;
     auto it = h.plans.find(key);
     if (it == h.plans.end()) {
-      if (!make_plan<BITS, MT8>(h, M, p)) return cudaErrorInvalidConfiguration;
-      cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      if constexpr (MT8 == 1)
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (!make_plan(h, M, p)) return cudaErrorInvalidConfiguration;
+      cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if constexpr (MT8 == 1) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      }
       if (e != cudaSuccess) return e;
       std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
       std::memcpy(v.data(), &p, sizeof(SmallPlan));
@@ -748,7 +797,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  if (!h.identity) {
+  if (!h.identity && !p.gather) {
     cudaLaunchConfig_t gcfg = {};
     const long total = (long)M * h.Kr;
     gcfg.gridDim = dim3((unsigned)std::min<long>((total + 255) / 256, 2L * h.sm_count));
@@ -764,7 +813,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   }
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
-                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs};
+                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
@@ -772,9 +821,13 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if constexpr (MT8 == 1)
-    if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16>, args, h.wr_map);
-  return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8>, args, h.wr_map);
+  if constexpr (MT8 == 1) {
+    if (p.gather)
+      return p.cw == 16 ? cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true>, args, h.wr_map)
+                        : cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, true>, args, h.wr_map);
+    if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false>, args, h.wr_map);
+  }
+  return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false>, args, h.wr_map);
 }
 
 template <typename T, int BITS>
@@ -794,7 +847,12 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 
 }  // namespace
 
-int small_m_launches(const Handle& h, int M) { return M > 0 ? (h.identity ? 1 : 2) : 0; }
+int small_m_launches(const Handle& h, int M) {
+  if (M <= 0) return 0;
+  if (h.identity) return 1;
+  SmallPlan p{};
+  return (make_plan(h, M, p) && p.gather) ? 1 : 2;
+}
 
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
   if (h.dtype == GPTQ_BF16) return launch_dtype<__nv_bfloat16>(h, x, y, M, st);
