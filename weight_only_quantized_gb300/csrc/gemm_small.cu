@@ -186,7 +186,17 @@ __device__ __forceinline__ uint32_t operand(const LaneWords<BITS>& lw, int p, ui
 template <typename T, int BITS>
 __device__ __forceinline__ uint32_t operand_raw(const LaneWords<BITS>& lw, int p) {
   constexpr uint32_t M2 = Magic<T>::bits * 0x00010001u;
-  if constexpr (BITS == 3) {
+  if constexpr (BITS == 4 && std::is_same<T, __half>::value) {
+    // fp16 holds 10 mantissa bits, so the odd nibbles need no shift: masked in place they read as
+    // 1024 + 16 q, and one exact fma (x 1/16 + 960) makes 1024 + q; one shift by 8 serves the
+    // upper two nibbles.  Per word one shift instead of three (the integer pipe is the busy one).
+    const uint32_t w = (p % 4) < 2 ? lw.w[p / 4] : (lw.w[p / 4] >> 8);
+    if ((p % 2) == 0) return and_or(w, 0x000F000Fu, M2);
+    const uint32_t v = and_or(w, 0x00F000F0u, M2);
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(v), "r"(0x2C002C00u), "r"(0x63806380u));
+    return d;
+  } else if constexpr (BITS == 3) {
     const uint32_t lo = and_or(lw.w[p / 8] >> (2 * (p % 8)), 0x00030003u, M2);
     const uint32_t hi = p <= 2 ? (lw.w[2] << (2 - p)) : (lw.w[2] >> (p - 2));
     return and_or(hi, 0x00040004u, lo);
