@@ -284,6 +284,8 @@ struct SmallArgs {
   int gather;
   int o_pm;         // int32 [Kr] copy of perm (-1: pad row)
   int o_raw;        // the caller's x rows, [M][K] as given
+  int cg_async;     // 1: the producer bulk-copies the chunk-group table (CTAs that own a whole SM, whose
+                    // start is not hidden behind the previous call); 0: every thread loads it at start
 };
 
 template <int CW>
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   auto empty = [&](int i) { return bar0 + 8u * (rd + i); };
   auto hfull = [&](int i) { return bar0 + 8u * (2 * rd + i); };
   auto hempty = [&](int i) { return bar0 + 8u * (2 * rd + 2 + i); };
+  const uint32_t cgfull = bar0 + 8u * (2 * rd + 4);   // the chunk-group table has landed
   const int32_t* pm = reinterpret_cast<const int32_t*>(smem + a.o_pm);
   uint8_t* rawx = smem + a.o_raw;
   const int zs_bytes = a.span_max * kZsRow;
@@ -328,9 +331,15 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   if (tid == 0) {
     for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), kSPB); }
     for (int i = 0; i < 2; ++i) { mbar_init(hfull(i), 1); mbar_init(hempty(i), kCW); }
+    mbar_init(cgfull, 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < NB * 4; i += kThreadsS) cg[i] = __ldg(&a.cgid[i]);
+  // A CTA that owns a whole SM starts only when the previous call's CTA there has left, so its
+  // chunk-group table comes in by one bulk copy from the producer (below) and the weight stream
+  // starts without a global round trip first; a half-SM CTA starts beside the previous call's and
+  // loads the table directly.
+  if (!a.cg_async)
+    for (int i = tid; i < NB * 4; i += kThreadsS) cg[i] = __ldg(&a.cgid[i]);
   __syncthreads();
 
   // Blocks of panel p, and the first group a panel touches (cgid ascends in the sorted order).
@@ -348,6 +357,11 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     int s_issued = 0;               // weight stages issued
     int q = 0;                      // segments (tile, panel) started
     int s_sent = 0, q_sent = 0;     // stages and segment headers actually issued
+    if (a.cg_async && go) {         // handle data, independent of the previous grid
+      mbar_arrive_expect_tx(cgfull, (uint32_t)NB * 16u);
+      bulk_g2s(smem_u32(cg), a.cgid, (uint32_t)NB * 16u, cgfull);
+    }
+    const bool cg_sent = a.cg_async && go != 0;
 
     for (int ti = T0; ti < T1; ++ti) {
       for (int p = 0; p < a.npanel; ++p, ++q) {
@@ -355,20 +369,6 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
         const int hs = q & 1;
         if (q >= 2) mbar_wait_poison(hempty(hs), ((q >> 1) - 1) & 1, limit);
         go &= limit != 0 ? 1u : 0u;   // after a timeout nothing more is issued
-        const int gf = cg[4 * p * a.pb], gl = cg[4 * (p * a.pb + nb) - 1];
-        const bool load_x = !a.single || q == 0;
-        const uint32_t zs_tx = (uint32_t)(gl - gf + 1) * kZsRow;
-        // x bytes: the staged rows, or (gathering) perm and the caller's rows as given
-        const uint32_t x_tx = !load_x ? 0u : GATHER ? (uint32_t)a.Kr * 4u + (uint32_t)a.M * a.ldx * 2u
-                                                    : (uint32_t)a.M * nb * 256u;
-        if (go) {
-          mbar_arrive_expect_tx(hfull(hs), zs_tx + x_tx);
-          bulk_g2s(smem_u32(zsreg + hs * zs_bytes), a.zst + ((size_t)ti * a.G + gf) * kZsRow, zs_tx, hfull(hs));
-          if (GATHER && load_x)     // handle data, before the wait on the previous grid
-            bulk_g2s(smem_u32(pm), a.perm, (uint32_t)a.Kr * 4u, hfull(hs));
-        }
-        q_sent += go ? 1 : 0;
-        // weights of the first segment (up to 4 stages) go out before x; x waits for the previous grid
         const int nst = (nb + kSPB - 1) / kSPB;
         int j = 0;
         auto issue_stage = [&](int l) {
@@ -386,9 +386,29 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           s_sent += go ? 1 : 0;
           ++s_issued;
         };
-        if (load_x) {
-          const int pre = waited ? 0 : min(nst, min(rd, 4));
+        if (q == 0) {
+          // weights of the first segment (up to 4 stages) need neither the table nor the previous
+          // grid: they go out first
+          const int pre = min(nst, min(rd, 4));
           for (; j < pre; ++j) issue_stage(j);
+          if (a.cg_async) mbar_wait_poison(cgfull, 0u, limit);
+          go &= limit != 0 ? 1u : 0u;
+        }
+        const int gf = cg[4 * p * a.pb], gl = cg[4 * (p * a.pb + nb) - 1];
+        const bool load_x = !a.single || q == 0;
+        const uint32_t zs_tx = (uint32_t)(gl - gf + 1) * kZsRow;
+        // x bytes: the staged rows, or (gathering) perm and the caller's rows as given
+        const uint32_t x_tx = !load_x ? 0u : GATHER ? (uint32_t)a.Kr * 4u + (uint32_t)a.M * a.ldx * 2u
+                                                    : (uint32_t)a.M * nb * 256u;
+        if (go) {
+          mbar_arrive_expect_tx(hfull(hs), zs_tx + x_tx);
+          bulk_g2s(smem_u32(zsreg + hs * zs_bytes), a.zst + ((size_t)ti * a.G + gf) * kZsRow, zs_tx, hfull(hs));
+          if (GATHER && load_x)     // handle data, before the wait on the previous grid
+            bulk_g2s(smem_u32(pm), a.perm, (uint32_t)a.Kr * 4u, hfull(hs));
+        }
+        q_sent += go ? 1 : 0;
+        if (load_x) {
+          // x waits for the previous grid
           if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
           if (go) {
             if constexpr (GATHER) {
@@ -413,6 +433,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int s = first; s < s_sent; ++s) mbar_wait_poison(full(s & (rd - 1)), (uint32_t)((s >> lg) & 1), drain);
     for (int qq = q_sent > 2 ? q_sent - 2 : 0; qq < q_sent; ++qq)
       mbar_wait_poison(hfull(qq & 1), (uint32_t)((qq >> 1) & 1), drain);
+    if (cg_sent) mbar_wait_poison(cgfull, 0u, drain);
     if ((limit == 0 || drain == 0) && lane == 0) atomicExch(a.err, DEV_ERR_TIMEOUT);
     return;
   }
@@ -467,6 +488,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
         for (int r = 0; r < 4; ++r) xsp[mt][r] = 0.f;
   };
+  if (a.cg_async && !mbar_wait(cgfull, 0u)) ok = false;   // the chunk-group table (no block runs without it)
   int s_base = 0;
   int q = 0;
   for (int ti = T0; ti < T1; ++ti) {
@@ -707,7 +729,7 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
   int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw,
-      gather, o_pm, o_raw;
+      gather, o_pm, o_raw, cg_async;
 };
 
 // Layout for codes of `bits` bits and MT8 m-tiles; with_gather adds the perm copy.
@@ -746,14 +768,16 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const int xs_bytes = NB * 8 * mt8 * 4;      // x sums per block, reused by every tile after the first
   const int pm_bytes = p.gather ? h.Kr * 4 : 0;
   const int raw_bytes = p.gather ? M * h.K * 2 : 0;
-  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + 4 * 8 + 16;
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + 5 * 8 + 16;
   const int SB = kSPB * bits * 512;
   int budget = target - fixed - 128;
   int rd = budget / (SB + 16);
   if (rd < 4) {   // large tables: take up to a whole SM's shared memory
+    target = kSmemFull;
     budget = kSmemFull - fixed - 128;
     rd = budget / (SB + 16);
   }
+  p.cg_async = target == kSmemFull ? 1 : 0;
   if (rd < 2) return false;
   rd = std::min(rd, 128);
   p.lg_rd = 0;
@@ -767,7 +791,7 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   p.o_pm = p.o_xs + xs_bytes;
   p.o_raw = p.o_pm + pm_bytes;
   p.o_bar = p.o_raw + raw_bytes;
-  p.smem = p.o_bar + (2 * rdp + 4) * 8 + 128;     // + alignment slack of the base
+  p.smem = p.o_bar + (2 * rdp + 5) * 8 + 128;     // + alignment slack of the base
   return p.smem <= 227 * 1024;
 }
 
@@ -823,7 +847,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   }
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
-                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw};
+                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
