@@ -64,9 +64,9 @@ typedef enum { GPTQ_PATH_AUTO = 0, GPTQ_PATH_SMALL_M = 1, GPTQ_PATH_LARGE_M = 2 
  *   qzeros_rows/cols     GPTQ-003: qzeros_cols == out_features/32*bits; out_features must also be
  *                        a multiple of 32 so that the floor in that rule is exact   (else SHAPE)
  *                        qzeros_rows must equal G = ceil(in_features/group_size), or 1 when
- *                        group_size == -1 ("one group covering in_features")       (else SHAPE)
+ *                        group_size == -1 (a single group spans all of K)           (else SHAPE)
  *   scales_rows/cols     must be [G, out_features]                                  (else SHAPE)
- *   g_idx_len            GPTQ-004: must equal in_features, or be 0 for "no g_idx" (else SHAPE)
+ *   g_idx_len            GPTQ-004: must equal in_features, or be 0 without g_idx (else SHAPE)
  *   group_size           -1 or >= 1                                          (else INVALID_ARG)
  * On GPTQ_OK, *in_features and *out_features (if non-NULL) receive K and N.
  */

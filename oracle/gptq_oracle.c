@@ -20,7 +20,7 @@
  * double, in ascending original k, one accumulator per output, with -ffp-contract=off.
  *
  * Readings of points the pages leave open (each also listed in the design notes):
- *   - 3-bit words: the Reader only says "inverse of the 10 / split / 10 loop in pack()".
+ *   - 3-bit words: the Reader gives unpacking only as the inverse of pack()'s 10 / split / 10 loop.
  *     Reading: 32 consecutive codes share 3 consecutive words; codes 0-9 sit at bits 3j of
  *     word 0, code 10 has bits 0-1 at word-0 bits 30-31 and bit 2 at word-1 bit 0, codes
  *     11-20 at word-1 bits 1+3(j-11), code 21 has bit 0 at word-1 bit 31 and bits 1-2 at
@@ -29,8 +29,8 @@
  *   - zeros: z = stored + 1 with no wrap (GPTQ-006), so z is in [1, 2^bits].
  *   - group_size = -1: one group, g_idx = 0 for every k.  g_idx = NULL means k // group_size.
  *
- * Runtime layout (oracle_runtime_layout) is this library's own kernel-private format, the
- * "runtime ABI" that the GPTQModel "Kernel Backends Reference" page separates from the
+ * Runtime layout (oracle_runtime_layout) is this library's own kernel-private format: the
+ * kernel-side layout that the GPTQModel "Kernel Backends Reference" page keeps apart from the
  * checkpoint layout.  Its definition is written out in that function's comment.
  */
 #include <stdint.h>

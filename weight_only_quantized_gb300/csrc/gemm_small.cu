@@ -1,35 +1,34 @@
 // Small-M GEMM (decode, M <= 16): a persistent weight stream at HBM speed.
 //
-// mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin, Machete": at small M "only the
-// weight bytes matter" (opening section); the quantised weight only pays if it stays packed
-// until the registers that feed the tensor core; a group scale cannot be hoisted out of the k
-// reduction (section on the LOP3 dequant and the scale); for tiny M the lever is every SM
-// streaming weights at once, with the skinny operand in the MMA's N slot (swap-AB, section
-// "Where the batch-size crossover is" and the M-bucketed dispatch discussion).
+// mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin, Machete": at small M the
+// call time is set by the bytes of the packed weights (opening section); the quantised weight only
+// pays if it stays packed until the registers that feed the tensor core; a group scale cannot be
+// hoisted out of the k reduction (section on the LOP3 dequant and the scale); for tiny M the lever
+// is every SM streaming weights at once, with the skinny operand in the MMA's N slot (swap-AB,
+// section "Where the batch-size crossover is" and the M-bucketed dispatch discussion).
 //
 // Design on sm_103a:
 //  * One CTA per SM, each owning a balanced run of 32-column tiles.  For every tile it streams
-//    the 128-row blocks of packed codes with one 2-D TMA box per block (its bits vectors of 512
-//    bytes; 512-byte bulk copies were issue-bound) into a ring of stages several tens of KB deep, so each SM keeps enough bytes
-//    in flight to saturate its share of HBM from the first microsecond.  One producer warp issues
-//    the copies; eight consumer warps take the blocks of a tile round robin.
+//    the 128-row blocks of packed codes, four blocks per 2-D TMA box (8 KB at 4 bits; smaller
+//    copies were issue-bound), into a ring of stages several tens of KB deep, with an evict-first
+//    L2 policy.  One producer warp issues the copies; 8 or 16 consumer warps take the blocks of a
+//    tile round robin.
 //  * Programmatic dependent launch: the producer starts the weight stream (handle-owned data),
 //    and only then waits (griddepcontrol.wait) for the previous grid before it copies x; the
-//    consumers write y only after x has arrived.  The CTA needs at most half an SM's shared
-//    memory, so the next call's CTAs start streaming while this call finishes.
+//    consumers write y only after x has arrived.  A short CTA needs at most half an SM, so the
+//    next call's CTAs start streaming while this call finishes.
 //  * x is staged per K-panel (all of K when it fits) by bulk copies into rows 64 bytes apart
-//    modulo 128, so a lane's 8-byte fragment load meets at most one other lane on its banks.
-//    With act-order, a small gather kernel first writes x in sorted k order into the handle's
-//    workspace.
+//    modulo 128, so a lane's fragment loads meet no other lane on their banks.  With act-order,
+//    x is put in sorted k order by the consumers from a copy of the caller's rows (M <= 2) or by
+//    a small gather kernel into the handle's workspace.
 //  * Zeros and scales come from a tile-major copy of the runtime layout (per tile and group 32
 //    zero bytes and 32 scales, permuted so that the four columns of a lane are adjacent): one
-//    bulk copy per tile and panel, then two shared loads per lane per 32-row chunk.
+//    bulk copy per tile and panel, then two shared loads per lane per block.
 //  * mma.sync.m16n8k16 with swap-AB: A = weights (16 output features x 16 k), B = x^T (16 k x 8
-//    batch rows), fp32 accumulators; each chunk's partial sum is scaled into the total in fp32.
-//  * Conversion: one LOP3 puts two codes into the mantissas of a magic fp16 (1024) or bf16 (128)
-//    pair (exactly magic + code), one packed subtract of (magic + zero) leaves the exact integer
-//    code - zero.  8-bit codes with bf16 go through the 2^23 fp32 magic because bf16 holds
-//    128 + q exactly only for q < 128.
+//    batch rows), fp32 accumulators.  The codes go in as the exact values magic + code (one LOP3
+//    per pair of codes; fp16 1024 + q, bf16 128 + q) and the zero comes out once per block in fp32
+//    against the sum of x; the group scale multiplies that fp32 partial sum.  8-bit codes with bf16
+//    go through the 2^23 fp32 magic, because bf16 holds 128 + q exactly only for q < 128.
 //  * Every wait is bounded; a timeout sets the handle's error word, and the CTA drains its copies
 //    and exits.
 #include "internal.cuh"
@@ -92,18 +91,6 @@ __device__ __forceinline__ void mma16816_z(float (&c)[4], const uint32_t (&a)[4]
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
-template <typename T> __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b);
-template <> __device__ __forceinline__ uint32_t sub2<__half>(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-template <> __device__ __forceinline__ uint32_t sub2<__nv_bfloat16>(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
@@ -139,12 +126,11 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // 8-bit codes with bf16 activations go through fp32; every other case uses the fp16/bf16 magic.
 template <typename T, int BITS> constexpr bool kViaF32 = BITS == 8 && std::is_same<T, __nv_bfloat16>::value;
 
-// Zero point (stored + 1) in the form operand() subtracts.
+// Zero point (stored + 1) in the form operand() subtracts: 2^23 + z as fp32 bits, exact.
 template <typename T, int BITS>
 __device__ __forceinline__ uint32_t prep_zero(uint32_t stored) {
-  const uint32_t z = stored + 1u;
-  if constexpr (kViaF32<T, BITS>) return __float_as_uint(8388608.0f + (float)z);   // 2^23 + z, exact
-  else return (Magic<T>::bits + z) * 0x00010001u;                                   // magic + z, both halves
+  static_assert(kViaF32<T, BITS>, "the subtract form serves 8-bit codes with bf16 only");
+  return __float_as_uint(8388608.0f + (float)(stored + 1u));
 }
 
 // Codes go into the MMA as the exact values magic + code (bf16 128 + q, fp16 1024 + q) and the
@@ -161,25 +147,17 @@ template <typename T> constexpr uint32_t kOnes2 = std::is_same<T, __nv_bfloat16>
 // then 1 word of the 1-bit plane).
 template <int BITS> struct LaneWords { uint32_t w[BITS]; };
 
-// (code - zero) of pair p of this lane as a T2 register (low half = even k of the pair), exact.
+// (code - zero) of pair p of this lane as a bf16x2 register (low half = even k of the pair), exact:
+// 8-bit codes with bf16 (128 + q is not exact in bf16, so the fold-zero form does not apply); the
+// codes become 2^23 + q in fp32, the zero comes off there, and the integer rounds exactly to bf16.
 template <typename T, int BITS>
 __device__ __forceinline__ uint32_t operand(const LaneWords<BITS>& lw, int p, uint32_t zq) {
-  constexpr uint32_t M2 = Magic<T>::bits * 0x00010001u;
-  if constexpr (BITS == 3) {
-    const uint32_t lo = and_or(lw.w[p / 8] >> (2 * (p % 8)), 0x00030003u, M2);
-    const uint32_t hi = p <= 2 ? (lw.w[2] << (2 - p)) : (lw.w[2] >> (p - 2));
-    return sub2<T>(and_or(hi, 0x00040004u, lo), zq);
-  } else if constexpr (kViaF32<T, BITS>) {
-    const uint32_t codes = (lw.w[p / 2] >> (8 * (p % 2))) & 0x00FF00FFu;
-    const float zf = __uint_as_float(zq);
-    const float lo = __uint_as_float(0x4B000000u | (codes & 0xFFFFu)) - zf;
-    const float hi = __uint_as_float(0x4B000000u | (codes >> 16)) - zf;
-    return pack_bf16x2(lo, hi);
-  } else {
-    constexpr int F = 16 / BITS;
-    constexpr uint32_t mask = ((1u << BITS) - 1u) * 0x00010001u;
-    return sub2<T>(and_or(lw.w[p / F] >> (BITS * (p % F)), mask, M2), zq);
-  }
+  static_assert(kViaF32<T, BITS>, "the subtract form serves 8-bit codes with bf16 only");
+  const uint32_t codes = (lw.w[p / 2] >> (8 * (p % 2))) & 0x00FF00FFu;
+  const float zf = __uint_as_float(zq);
+  const float lo = __uint_as_float(0x4B000000u | (codes & 0xFFFFu)) - zf;
+  const float hi = __uint_as_float(0x4B000000u | (codes >> 16)) - zf;
+  return pack_bf16x2(lo, hi);
 }
 
 // magic + code of pair p (both halves), exact (the kFoldZero form).

@@ -34,7 +34,7 @@ struct Handle {
   uint8_t* zst = nullptr;    // [Np/32][G][96]: per 32-column tile and group, 32 stored zeros then
                              // 32 scales, column c at position (c % 8) * 4 + c / 8 (small-M path)
   std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)
-  alignas(64) CUtensorMap wr_map;   // wr as uint64 [Kr/128 * bits rows][2 Np]: one box = kSmallBlocksPerBox
+  CUtensorMap wr_map;               // wr as uint64 [Kr/128 * bits rows][2 Np]: one box = kSmallBlocksPerBox
                                     // blocks of one 32-column tile (small-M path)
   int32_t* err = nullptr;    // device error word: kernels set it when a bounded wait gives up
   // workspace
