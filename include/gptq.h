@@ -96,7 +96,7 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
  *            as the call returns; the handle holds its own copy in its runtime layout.
  *   out      receives the handle (set to NULL on failure).
  * The handle allocates its runtime layout (about K*N*bits/8 bytes plus 6*G*N) and a workspace
- * for gptq_gemm calls with M <= 16; gptq_reserve enlarges the workspace.  The handle is
+ * for gptq_gemm calls with M <= 32; gptq_reserve enlarges the workspace.  The handle is
  * immutable: after any change to the weights, build a new one.
  * Errors: INVALID_ARG, UNSUPPORTED, SHAPE, ALIGNMENT, DEVICE, INVALID_GIDX, CUDA.
  */
@@ -107,8 +107,8 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
 /*
  * Make gptq_gemm calls with M <= max_M possible without any allocation inside gptq_gemm.
  * Only a handle whose g_idx order is not the identity (act-order, or groups whose sizes are
- * not multiples of 32) needs workspace above M = 16: max_M * K_sorted activation elements for
- * the permuted copy of x that the large-M kernel reads.  Allocates (cudaMalloc) outside any
+ * not multiples of 32) needs workspace above M = 32: max_M * K_sorted activation elements for
+ * the permuted copy of x that the kernels read.  Allocates (cudaMalloc) outside any
  * stream capture; never shrinks.  Errors: INVALID_ARG, CUDA.
  */
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);

@@ -63,10 +63,12 @@ def test_large_path_one_hot_exact(dtype):
         assert np.array_equal(y[i], torch.from_numpy(W[:, k]).to(tdt).float().numpy()), k
 
 
-def test_auto_dispatch_uses_large_path_above_16():
+def test_launch_counts_per_path():
     spec = synth.LayerSpec(256, 256, 4, 128)
     h = repack(synth.make_checkpoint(spec))
     assert gptq.gptq_gemm_launches(h, 16) == 1
+    assert gptq.gptq_gemm_launches(h, 28) == 1          # small-M kernel, four m-tiles
+    assert gptq.gptq_gemm_launches(h, 29) == 1          # tcgen05 kernel
     assert gptq.gptq_gemm_launches(h, 17, gptq.PATH_LARGE_M) == 1
     spec = synth.LayerSpec(256, 256, 4, 128, True)
     h = repack(synth.make_checkpoint(spec))

@@ -110,11 +110,32 @@ def test_invalid_g_idx_value_is_reported():
     assert ei.value.status == 4 and "g_idx[77]" in str(ei.value)
 
 
+@pytest.mark.parametrize("spec", SPECS[:4] + SPECS[5:8], ids=_id)
+@pytest.mark.parametrize("M", [17, 24, 32])
+def test_small_path_four_m_tiles(spec, M):
+    """The small-M kernel forced at 17 <= M <= 32 (four 8-row m-tiles)."""
+    ck = synth.make_checkpoint(spec, seed=spec.K + 3 * spec.N + M)
+    h = repack(ck)
+    x = synth.make_x(M, spec.K, spec.dtype, seed=M + 11)
+    compare(run_gemm(h, x, spec.N, gptq.PATH_SMALL_M), oracle_y(ck, x))
+    gptq.gptq_device_status(h)
+
+
+def test_small_path_refuses_m_above_its_tiles():
+    spec = synth.LayerSpec(256, 256, 4, 128)
+    h = repack(synth.make_checkpoint(spec))
+    x = torch.zeros(33, 256, dtype=torch.float16, device="cuda")
+    y = torch.zeros(33, 256, dtype=torch.float16, device="cuda")
+    with pytest.raises(gptq.GptqError) as e:
+        gptq.gptq_gemm_path(h, x, y, gptq.PATH_SMALL_M)
+    assert e.value.status == 1                          # INVALID_ARG
+
+
 def test_workspace_required_above_reserve():
     spec = synth.LayerSpec(256, 256, 4, 128, True)
     h = repack(synth.make_checkpoint(spec))
     info = gptq.gptq_get_info(h)
-    assert info.identity == 0 and info.reserved_M == 16
+    assert info.identity == 0 and info.reserved_M == 32
     x = torch.zeros(40, 256, dtype=torch.float16, device="cuda")
     y = torch.zeros(40, 256, dtype=torch.float16, device="cuda")
     try:

@@ -13,10 +13,12 @@ thread_local std::string g_last_error;
 constexpr int kMaxK = 1 << 17;        // in_features limit (index arithmetic and repack cost)
 constexpr int kMaxN = 1 << 18;        // out_features limit
 constexpr int kMaxGroups = 1 << 16;
-// Largest M routed to the small-M (mma.sync weight-streaming) kernel by gptq_gemm.  At M <= 16
-// the layer is HBM-bound on GB300 (ridge M* = P * 4.125 / (16 * BW) ~ 72 for 4-bit group 128)
-// and the swap-AB mma.sync kernel keeps every SM streaming weights.
-constexpr int kSmallMMax = 16;
+// Largest M routed to the small-M (mma.sync weight-streaming) kernel by gptq_gemm.  Up to M = 16
+// the layer is HBM-bound on GB300 (ridge M* = P * 4.125 / (16 * BW) ~ 72 for 4-bit group 128) and
+// the swap-AB mma.sync kernel keeps every SM streaming weights.  With four m-tiles it also beats
+// the tcgen05 kernel up to M = 28 (measured: 22 vs 28 us at M = 24 on a 4096 x 14336 layer, 84 vs
+// 110 us on 8192 x 28672); above that its x panels shrink to four blocks and it falls behind.
+constexpr int kSmallMMax = 28;
 }  // namespace
 
 gptq_status_t fail(gptq_status_t s, const std::string& msg) {
@@ -93,6 +95,12 @@ static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, 
                                       "order is not the identity and only M <= " + std::to_string(h.reserved_M) + " is reserved");
     e = launch_gemm_large(h, x, y, M, st);
   } else {
+    if (M > small_m_max())
+      return fail(GPTQ_ERR_INVALID_ARG, "M = " + std::to_string(M) + " is above the small-M kernel's " +
+                                            std::to_string(small_m_max()) + " rows");
+    if (!h.identity && M > h.reserved_M && small_m_launches(h, M) == 2)
+      return fail(GPTQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs gptq_reserve(h, M): the handle's g_idx "
+                                      "order is not the identity and only M <= " + std::to_string(h.reserved_M) + " is reserved");
     e = launch_gemm_small(h, x, y, M, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "gptq_gemm launch");
@@ -185,7 +193,7 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
   s = build_runtime(*h, qweight, qzeros, scales, g_idx, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
-  s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 16);
+  s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 32);
   if (s != GPTQ_OK) { free_handle(h); return s; }
   *out = reinterpret_cast<gptq_handle_t>(h);
   return GPTQ_OK;

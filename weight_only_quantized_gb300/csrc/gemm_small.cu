@@ -1,4 +1,4 @@
-// Small-M GEMM (decode, M <= 16): a persistent weight stream at HBM speed.
+// Small-M GEMM (decode, M <= 32): a persistent weight stream at HBM speed.
 //
 // mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin, Machete": at small M the
 // call time is set by the bytes of the packed weights (opening section); the quantised weight only
@@ -776,7 +776,7 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
 // The plan: act-order handles gather x in the GEMM kernel at M <= 2 when x is staged once and the
 // weight ring keeps at least eight stages; otherwise a pre-pass gathers x into the workspace.
 bool make_plan(const Handle& h, int M, SmallPlan& p) {
-  const int mt8 = M <= 8 ? 1 : 2;
+  const int mt8 = M <= 8 ? 1 : M <= 16 ? 2 : 4;
   if (!h.identity && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
   return plan_layout(h, M, h.bits, mt8, false, p);
 }
@@ -844,7 +844,10 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
 
 template <typename T, int BITS>
 cudaError_t launch_bits(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  return M <= 8 ? launch_t<T, BITS, 1>(h, x, y, M, st) : launch_t<T, BITS, 2>(h, x, y, M, st);
+  if (M <= 8) return launch_t<T, BITS, 1>(h, x, y, M, st);
+  if (M <= 16) return launch_t<T, BITS, 2>(h, x, y, M, st);
+  if (M <= 32) return launch_t<T, BITS, 4>(h, x, y, M, st);
+  return cudaErrorInvalidValue;
 }
 
 template <typename T>
@@ -858,6 +861,8 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 }
 
 }  // namespace
+
+int small_m_max() { return 32; }
 
 int small_m_launches(const Handle& h, int M) {
   if (M <= 0) return 0;

@@ -75,6 +75,7 @@ gptq_status_t cuda_fail(cudaError_t e, const char* what);
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
+int small_m_max();   // largest M the small-M kernel covers (four m-tiles of 8 rows)
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
 
 // Large-M path: tcgen05 / TMEM / TMA kernel (plus an x-permute pre-pass when not identity).
