@@ -395,3 +395,123 @@ int oracle_runtime_layout(const int32_t* qweight, const int32_t* qzeros, const u
     }
   return ORACLE_OK;
 }
+
+/*
+ * AutoAWQ GEMM checkpoints, [P4] ch. 39, section "AWQ" (its pack_awq / unpack_awq /
+ * from_checkpoint description): 4-bit codes, eight to an int32 word along the OUTPUT
+ * dimension in the interleaved order 0 2 4 6 1 3 5 7 -- nibble j (bits 4j..4j+3) of word w
+ * holds output column 8w + order[j], so output 1 sits in bits 16-19.  qweight is [K, N/8],
+ * qzeros [G, N/8] packed the same way, scales [G, N]; from_checkpoint builds the offset as
+ * -zero * scale with the stored zero itself (no +1), and groups are consecutive runs of
+ * group_size input rows (the format carries no g_idx):
+ *   W[n, k] = (q[k, n] - z[g, n]) * scales[g, n],  g = k // group_size.
+ */
+static const int awq_order[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+/* Nibble of word row[n / 8] that holds output column n. */
+static uint32_t awq_code(const int32_t* row, long n) {
+  int o = (int)(n % 8), j = 0;
+  while (awq_order[j] != o) ++j;
+  return ((uint32_t)row[n / 8] >> (4 * j)) & 0xFu;
+}
+
+/* packed int32 [rows, N/8] -> codes uint8 [rows][N] */
+int oracle_awq_unpack(const int32_t* packed, int rows, int N, uint8_t* out) {
+  if (rows <= 0 || N <= 0 || N % 8) return ORACLE_EINVAL;
+  for (long r = 0; r < rows; ++r)
+    for (long n = 0; n < N; ++n) out[r * N + n] = (uint8_t)awq_code(packed + r * (N / 8), n);
+  return ORACLE_OK;
+}
+
+/* codes uint8 [rows][N] (values 0..15) -> packed int32 [rows, N/8], the inverse of oracle_awq_unpack */
+int oracle_awq_pack(const uint8_t* codes, int rows, int N, int32_t* packed) {
+  if (rows <= 0 || N <= 0 || N % 8) return ORACLE_EINVAL;
+  for (long r = 0; r < rows; ++r)
+    for (long w = 0; w < N / 8; ++w) {
+      uint32_t word = 0;
+      for (int j = 0; j < 8; ++j) word |= ((uint32_t)codes[r * N + 8 * w + awq_order[j]] & 0xFu) << (4 * j);
+      packed[r * (N / 8) + w] = (int32_t)word;
+    }
+  return ORACLE_OK;
+}
+
+static void awq_dequant_row(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                            int K, int N, int group_size, long n, float* row) {
+  for (long k = 0; k < K; ++k) {
+    long g = group_size == -1 ? 0 : k / group_size;
+    float q = (float)awq_code(qweight + k * (N / 8), n);
+    float z = (float)awq_code(qzeros + g * (N / 8), n);
+    float s = half_bits_to_float(scales[g * N + n], dtype);
+    row[k] = (q - z) * s;
+  }
+}
+
+static int awq_shape_ok(int K, int N, int group_size) {
+  if (K <= 0 || K % 32 || N <= 0 || N % 32) return 0;
+  if (group_size != -1 && (group_size <= 0 || group_size > K)) return 0;
+  return 1;
+}
+
+/* Dense W float32 [N][K] of an AWQ checkpoint. */
+int oracle_awq_dequant(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                       int K, int N, int group_size, float* W) {
+  if (!awq_shape_ok(K, N, group_size)) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(static)
+  for (long n = 0; n < N; ++n) awq_dequant_row(qweight, qzeros, scales, dtype, K, N, group_size, n, W + n * (long)K);
+  return ORACLE_OK;
+}
+
+/* y[r][c] = sum_k x[rows[r]][k] * W[cols[c]][k] for an AWQ checkpoint, as oracle_linear. */
+int oracle_awq_linear(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                      int K, int N, int group_size, const uint16_t* x, int M, const int32_t* rows, int nrows,
+                      const int32_t* cols, int ncols, double* y) {
+  if (!awq_shape_ok(K, N, group_size)) return ORACLE_EINVAL;
+  for (int r = 0; r < nrows; ++r) if (rows[r] < 0 || rows[r] >= M) return ORACLE_EINVAL;
+  for (int c = 0; c < ncols; ++c) if (cols[c] < 0 || cols[c] >= N) return ORACLE_EINVAL;
+  float* xf = (float*)malloc(sizeof(float) * (size_t)nrows * K);
+  if (!xf) return ORACLE_EINVAL;
+  for (long r = 0; r < nrows; ++r)
+    for (long k = 0; k < K; ++k) xf[r * K + k] = half_bits_to_float(x[(long)rows[r] * K + k], dtype);
+  int fail = 0;
+#pragma omp parallel
+  {
+    float* row = (float*)malloc(sizeof(float) * (size_t)K);
+    if (!row) {
+#pragma omp atomic write
+      fail = 1;
+    } else {
+#pragma omp for schedule(static)
+      for (long c = 0; c < ncols; ++c) {
+        awq_dequant_row(qweight, qzeros, scales, dtype, K, N, group_size, cols[c], row);
+        for (long r = 0; r < nrows; ++r) {
+          double acc = 0.0;
+          const float* xr = xf + r * K;
+          for (long k = 0; k < K; ++k) acc += (double)xr[k] * (double)row[k];
+          y[r * ncols + c] = acc;
+        }
+      }
+      free(row);
+    }
+  }
+  free(xf);
+  return fail ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/*
+ * The same codes and zero fields in GPTQ packing (codes along K, zero fields along N), for the
+ * runtime-layout comparison: the zero field carries the AWQ zero itself, which a handle built
+ * from an AWQ checkpoint reads with a zero offset of 0 (GPTQ fields read with offset 1).
+ * qweight_gptq int32 [K/8, N]; qzeros_gptq int32 [G, N/8].
+ */
+int oracle_awq_to_gptq_fields(const int32_t* qweight, const int32_t* qzeros, int K, int N, int group_size,
+                              int32_t* qweight_gptq, int32_t* qzeros_gptq) {
+  if (!awq_shape_ok(K, N, group_size)) return ORACLE_EINVAL;
+  int G = oracle_num_groups(K, group_size);
+  memset(qweight_gptq, 0, sizeof(int32_t) * (size_t)K / 8 * N);
+  memset(qzeros_gptq, 0, sizeof(int32_t) * (size_t)G * (N / 8));
+  for (long k = 0; k < K; ++k)
+    for (long n = 0; n < N; ++n) put_code(qweight_gptq + n, N, k, 4, awq_code(qweight + k * (N / 8), n));
+  for (long g = 0; g < G; ++g)
+    for (long n = 0; n < N; ++n) put_code(qzeros_gptq + g * (N / 8), 1, n, 4, awq_code(qzeros + g * (N / 8), n));
+  return ORACLE_OK;
+}

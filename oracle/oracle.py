@@ -57,6 +57,11 @@ def lib():
                 "oracle_runtime_dims": [P, I, I, I, P, P],
                 "oracle_runtime_layout": [P, P, P, P, I, I, I, I, P, P, P, P, P],
                 "oracle_num_threads": [],
+                "oracle_awq_unpack": [P, I, I, P],
+                "oracle_awq_pack": [P, I, I, P],
+                "oracle_awq_dequant": [P, P, P, I, I, I, I, P],
+                "oracle_awq_linear": [P, P, P, I, I, I, I, P, I, P, I, P, I, P],
+                "oracle_awq_to_gptq_fields": [P, P, I, I, I, P, P],
             }
             for name, args in sigs.items():
                 f = getattr(L, name)
@@ -202,3 +207,57 @@ def num_threads() -> int:
 
 def half_to_float(bits_u16: int, dtype: str) -> float:
     return lib().oracle_half_to_float(bits_u16, DT[dtype])
+
+
+# ---- AutoAWQ GEMM checkpoints (4-bit, packed along the output dimension) ----
+
+def awq_unpack(packed) -> np.ndarray:
+    """int32 [rows, N/8] in AWQ's interleaved order -> uint8 codes [rows, N]."""
+    pk = _np(packed, np.int32)
+    rows, N = pk.shape[0], pk.shape[1] * 8
+    out = np.empty((rows, N), np.uint8)
+    _check(lib().oracle_awq_unpack(_p(pk), rows, N, _p(out)), "awq_unpack")
+    return out
+
+
+def awq_pack(codes) -> np.ndarray:
+    c = _np(codes, np.uint8)
+    rows, N = c.shape
+    out = np.empty((rows, N // 8), np.int32)
+    _check(lib().oracle_awq_pack(_p(c), rows, N, _p(out)), "awq_pack")
+    return out
+
+
+def awq_dequant(qweight, qzeros, scales, group_size: int, dtype: str) -> np.ndarray:
+    """Dense W float32 [N, K] of an AWQ checkpoint."""
+    qw, qz, sc = _np(qweight, np.int32), _np(qzeros, np.int32), _np(scales, np.uint16)
+    K, N = qw.shape[0], qw.shape[1] * 8
+    W = np.empty((N, K), np.float32)
+    _check(lib().oracle_awq_dequant(_p(qw), _p(qz), _p(sc), DT[dtype], K, N, group_size, _p(W)), "awq_dequant")
+    return W
+
+
+def awq_linear(qweight, qzeros, scales, group_size: int, dtype: str, x, rows=None, cols=None) -> np.ndarray:
+    """y[rows][cols] = x[rows] . W[cols]^T in float64 for an AWQ checkpoint."""
+    qw, qz, sc = _np(qweight, np.int32), _np(qzeros, np.int32), _np(scales, np.uint16)
+    xx = _np(x, np.uint16)
+    K, N = qw.shape[0], qw.shape[1] * 8
+    M = xx.shape[0]
+    assert xx.shape[1] == K
+    r = np.arange(M, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, np.int32)
+    y = np.empty((len(r), len(c)), np.float64)
+    _check(lib().oracle_awq_linear(_p(qw), _p(qz), _p(sc), DT[dtype], K, N, group_size, _p(xx), M,
+                                   _p(r), len(r), _p(c), len(c), _p(y)), "awq_linear")
+    return y
+
+
+def awq_to_gptq_fields(qweight, qzeros, group_size: int) -> tuple[np.ndarray, np.ndarray]:
+    """The AWQ codes and zero fields in GPTQ packing (zero field = the AWQ zero itself)."""
+    qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
+    K, N = qw.shape[0], qw.shape[1] * 8
+    G = num_groups(K, group_size)
+    qwg = np.empty((K // 8, N), np.int32)
+    qzg = np.empty((G, N // 8), np.int32)
+    _check(lib().oracle_awq_to_gptq_fields(_p(qw), _p(qz), K, N, group_size, _p(qwg), _p(qzg)), "awq_to_gptq_fields")
+    return qwg, qzg

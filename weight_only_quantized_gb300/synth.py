@@ -95,6 +95,36 @@ def make_checkpoint(spec: LayerSpec, seed: int = 0) -> Checkpoint:
     return Checkpoint(spec, qweight, qzeros, scales, g_idx)
 
 
+@dataclasses.dataclass
+class AwqCheckpoint:
+    """An AutoAWQ GEMM layer (4-bit, codes packed eight to a word along the output dimension)."""
+    K: int
+    N: int
+    group_size: int
+    dtype: str                   # dtype of scales, x and y (the format ships fp16 scales)
+    qweight: torch.Tensor        # int32 [K, N/8]
+    qzeros: torch.Tensor         # int32 [G, N/8]
+    scales: torch.Tensor         # fp16/bf16 [G, N]
+
+    @property
+    def G(self) -> int:
+        return 1 if self.group_size == -1 else -(-self.K // self.group_size)
+
+
+def make_awq_checkpoint(K: int, N: int, group_size: int = 128, dtype: str = "fp16", seed: int = 0,
+                        scale_lo: float = 0.002, scale_hi: float = 0.01) -> AwqCheckpoint:
+    """Uniform random words again carry uniform independent 4-bit codes and zeros: in the AWQ
+    packing every nibble of a qweight or qzeros word is one field (only their order along the
+    output dimension differs from GPTQ).  Draw order: qweight words, qzeros words, scales."""
+    gen = torch.Generator().manual_seed(seed)
+    G = 1 if group_size == -1 else -(-K // group_size)
+    qweight = random_words(gen, (K, N // 8))
+    qzeros = random_words(gen, (G, N // 8))
+    scales = (torch.rand((G, N), generator=gen, dtype=torch.float64) * (scale_hi - scale_lo)
+              + scale_lo).to(_DTYPES[dtype])
+    return AwqCheckpoint(K, N, group_size, dtype, qweight, qzeros, scales)
+
+
 def make_x(M: int, K: int, dtype: str, seed: int = 1) -> torch.Tensor:
     gen = torch.Generator().manual_seed(seed)
     return torch.randn((M, K), generator=gen, dtype=torch.float32).to(_DTYPES[dtype])
