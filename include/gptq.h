@@ -114,6 +114,28 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
 
 /*
+ * Build a runtime handle from one AutoAWQ GEMM layer (inference.shantanugoel.com ch. 39
+ * "Quantized checkpoints", section "AWQ": the pack_awq / unpack_awq / from_checkpoint
+ * description).  The layer is 4-bit and has no g_idx; W[n, k] = (code[k, n] - zero[g, n]) *
+ * scale[g, n] with g = k / group_size and the zero read as stored (no +1).
+ *   qweight  device, int32 [K, N/8] row-major: eight 4-bit codes per word along the OUTPUT
+ *            dimension, nibble j (bits 4j..4j+3) of word w holding output 8w + order[j],
+ *            order = 0 2 4 6 1 3 5 7 (output 1 in bits 16-19).  4-byte aligned.
+ *   qzeros   device, int32 [G, N/8] row-major, packed the same way; the field is the zero.
+ *   scales   device, dtype [G, N] row-major (the format ships fp16; bf16 is accepted).  2-byte
+ *            aligned.
+ *   K, N, group_size, dtype, stream, out: as for gptq_repack (K % 32 == 0 and N % 32 == 0;
+ *            G = ceil(K/group_size), or 1 for group_size == -1).
+ * The handle is the same kind as gptq_repack's (sequential groups, so its sorted order is the
+ * identity when group_size is a multiple of 32) and serves every other call; gptq_get_info
+ * reports zero_offset = 0 for it.
+ * Errors: INVALID_ARG, UNSUPPORTED (dtype), SHAPE, ALIGNMENT, DEVICE, CUDA.
+ */
+gptq_status_t gptq_repack_awq(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                              int K, int N, int group_size, gptq_dtype_t dtype, void* stream,
+                              gptq_handle_t* out);
+
+/*
  * y = x . W^T for the handle's layer, enqueued on `stream`.
  *   x   device, dtype [M, K] row-major (row stride K elements), 16-byte aligned.
  *   y   device, dtype [M, N] row-major (row stride N elements), 16-byte aligned; x and y must
@@ -148,6 +170,7 @@ typedef struct {
   int identity;     /* 1 when the sorted order is k itself (no permutation, no padding)       */
   gptq_dtype_t dtype;
   int reserved_M;   /* largest M gptq_gemm accepts on every path without further reserve      */
+  int zero_offset;  /* zero = stored zero field + zero_offset: 1 (gptq_repack), 0 (gptq_repack_awq) */
   size_t weight_bytes;     /* runtime codes: K_sorted/128 * bits * N_padded * 16              */
   size_t device_bytes;     /* everything the handle holds on the device                      */
 } gptq_info_t;
@@ -158,7 +181,7 @@ gptq_status_t gptq_get_info(gptq_handle_t h, gptq_info_t* info);
  * Copy the runtime layout to host memory (synchronous), for checking the repack bit by bit.
  *   wr    host, info.weight_bytes bytes        perm  host, int32 [K_sorted]
  *   cgid  host, int32 [K_sorted/32]            s_r   host, dtype bits [G, N_padded]
- *   z_r   host, uint8 [G, N_padded] (stored zero = zero - 1)
+ *   z_r   host, uint8 [G, N_padded]: the checkpoint's zero field (GPTQ: zero - 1; AWQ: the zero)
  * Any pointer may be NULL to skip that buffer.  Errors: INVALID_ARG, CUDA.
  */
 gptq_status_t gptq_copy_runtime(gptq_handle_t h, void* wr, int32_t* perm, int32_t* cgid,

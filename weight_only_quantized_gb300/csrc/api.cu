@@ -31,7 +31,7 @@ gptq_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, cudaStream_t st);
+                            const int32_t* g_idx, bool awq, cudaStream_t st);
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -159,9 +159,13 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
   return GPTQ_OK;
 }
 
-gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
-                          int K, int N, int bits, int group_size, gptq_dtype_t dtype, void* stream,
-                          gptq_handle_t* out) {
+}  // extern "C"
+
+namespace gptq {
+// Argument checks shared by both checkpoint formats, then the handle and its runtime layout.
+static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                                 const int32_t* g_idx, int K, int N, int bits, int group_size, gptq_dtype_t dtype,
+                                 bool awq, void* stream, gptq_handle_t* out) {
   if (!out) return fail(GPTQ_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!qweight || !qzeros || !scales) return fail(GPTQ_ERR_INVALID_ARG, "qweight, qzeros and scales are required");
@@ -187,16 +191,31 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
   h->K = K; h->N = N; h->bits = bits; h->group_size = group_size; h->G = G;
   h->Np = (N + 255) / 256 * 256;
   h->dtype = dtype;
+  h->zoff = awq ? 0 : 1;
   cudaError_t ce = cudaMalloc(&h->err, sizeof(int32_t));
   if (ce == cudaSuccess) ce = cudaMemsetAsync(h->err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaMalloc(error word)"); }
-  s = build_runtime(*h, qweight, qzeros, scales, g_idx, static_cast<cudaStream_t>(stream));
+  s = build_runtime(*h, qweight, qzeros, scales, g_idx, awq, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
   s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 32);
   if (s != GPTQ_OK) { free_handle(h); return s; }
   *out = reinterpret_cast<gptq_handle_t>(h);
   return GPTQ_OK;
+}
+}  // namespace gptq
+
+extern "C" {
+
+gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
+                          int K, int N, int bits, int group_size, gptq_dtype_t dtype, void* stream,
+                          gptq_handle_t* out) {
+  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, stream, out);
+}
+
+gptq_status_t gptq_repack_awq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int K, int N,
+                              int group_size, gptq_dtype_t dtype, void* stream, gptq_handle_t* out) {
+  return repack_impl(qweight, qzeros, scales, nullptr, K, N, 4, group_size, dtype, true, stream, out);
 }
 
 gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
@@ -266,6 +285,7 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->K = h.K; info->N = h.N; info->bits = h.bits; info->group_size = h.group_size; info->G = h.G;
   info->K_sorted = h.Kr; info->N_padded = h.Np; info->identity = h.identity; info->dtype = h.dtype;
   info->reserved_M = h.reserved_M;
+  info->zero_offset = h.zoff;
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
                        (size_t)h.G * h.Np * 6 + h.xp_bytes;

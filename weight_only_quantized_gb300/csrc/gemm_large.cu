@@ -91,6 +91,7 @@ struct LargeArgs {
   const uint8_t* wr; const int32_t* cgid; const uint16_t* s_r; const uint8_t* z_r;
   void* y; int32_t* err;
   int M, N, Np, Kr, G;
+  int zoff;         // zero = stored byte + zoff (1: GPTQ fields; 0: AWQ fields)
 };
 
 __device__ __forceinline__ uint32_t and_or_l(uint32_t a, uint32_t b, uint32_t c) {
@@ -163,9 +164,10 @@ __device__ __forceinline__ uint32_t code_minus_zero(const Words<BITS>& lw, int p
   }
 }
 
+// Zero = stored byte + zoff (1 for GPTQ fields, stored minus one; 0 for AWQ fields).
 template <typename T, int BITS>
-__device__ __forceinline__ uint32_t prep_zero_l(uint32_t stored) {
-  const uint32_t z = stored + 1u;
+__device__ __forceinline__ uint32_t prep_zero_l(uint32_t stored, uint32_t zoff) {
+  const uint32_t z = stored + zoff;
   if constexpr (kF32Path<T, BITS>) return __float_as_uint(8388608.0f + (float)z);
   else return (MagicL<T>::bits + z) * 0x00010001u;
 }
@@ -489,13 +491,14 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDq) {
       // ---------------- dequantisers: thread owns weight row n0 + nrow ----------------
       const int nrow = 32 * (warp - kDqWarp0) + lane;
+      const uint32_t zoff = (uint32_t)a.zoff;
       uint32_t zq[4];
       for (int blk = 0; blk < nblocks && ok; ++blk) {
         const int ps = blk % PS;
         if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
         const uint8_t* stage = pk + ps * PKB;
   #pragma unroll
-        for (int c = 0; c < 4; ++c) zq[c] = prep_zero_l<T, BITS>(stage[PK_BYTES<BITS> + c * BN + nrow]);
+        for (int c = 0; c < 4; ++c) zq[c] = prep_zero_l<T, BITS>(stage[PK_BYTES<BITS> + c * BN + nrow], zoff);
         for (int h = 0; h < 2; ++h) {
           const int i = 2 * blk + h, ws = i % WS;
           if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
@@ -567,7 +570,7 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G};
+  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, 1);     // consecutive CTAs share a weight tile
   cfg.blockDim = dim3(kThreadsL);

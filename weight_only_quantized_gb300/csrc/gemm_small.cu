@@ -126,11 +126,11 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // 8-bit codes with bf16 activations go through fp32; every other case uses the fp16/bf16 magic.
 template <typename T, int BITS> constexpr bool kViaF32 = BITS == 8 && std::is_same<T, __nv_bfloat16>::value;
 
-// Zero point (stored + 1) in the form operand() subtracts: 2^23 + z as fp32 bits, exact.
+// Zero point (stored + zoff) in the form operand() subtracts: 2^23 + z as fp32 bits, exact.
 template <typename T, int BITS>
-__device__ __forceinline__ uint32_t prep_zero(uint32_t stored) {
+__device__ __forceinline__ uint32_t prep_zero(uint32_t stored, uint32_t zoff) {
   static_assert(kViaF32<T, BITS>, "the subtract form serves 8-bit codes with bf16 only");
-  return __float_as_uint(8388608.0f + (float)(stored + 1u));
+  return __float_as_uint(8388608.0f + (float)(stored + zoff));
 }
 
 // Codes go into the MMA as the exact values magic + code (bf16 128 + q, fp16 1024 + q) and the
@@ -264,6 +264,7 @@ struct SmallArgs {
   int o_raw;        // the caller's x rows, [M][K] as given
   int cg_async;     // 1: the producer bulk-copies the chunk-group table (CTAs that own a whole SM, whose
                     // start is not hidden behind the previous call); 0: every thread loads it at start
+  int zoff;         // zero = stored byte + zoff (1: GPTQ fields, stored minus one; 0: AWQ fields)
 };
 
 template <int CW>
@@ -437,6 +438,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   for (int mt = 0; mt < MT8; ++mt) xoff[mt] = (mval[mt] ? 8 * mt + g : 0) * a.x_row + 16 * t;
   uint32_t zq[4];                  // prepared zero (the subtract form)
   float zc[4];                     // magic + zero in fp32 (the kFoldZero form)
+  const float zsub = 8388608.0f - kMagicF<T> - (float)a.zoff;   // 2^23 + stored -> magic + zero
   float sc[4];
   // x sums of this lane's two batch columns (8 mt + 2t and + 1) over the chunks being folded
   float2 xsv[MT8];
@@ -543,11 +545,11 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
               for (int idx = 0; idx < 4; ++idx) {
                 if constexpr (kFoldZero<T, BITS>) {
-                  // magic + stored zero + 1 in fp32: one byte permute builds 2^23 + stored (exact),
+                  // magic + stored zero + zoff in fp32: one byte permute builds 2^23 + stored (exact),
                   // one add moves it (exact: integers below 2^24)
-                  zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - (8388608.0f - kMagicF<T> - 1.0f);
+                  zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - zsub;
                 } else {
-                  zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu);
+                  zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu, (uint32_t)a.zoff);
                 }
               }
               sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
@@ -825,7 +827,8 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   }
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
-                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async};
+                 p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
+                 h.zoff};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());

@@ -30,7 +30,8 @@ struct Handle {
   int32_t* perm = nullptr;   // [Kr], -1 for pad rows
   int32_t* cgid = nullptr;   // [Kr/32] group of each 32-row chunk
   uint16_t* s_r = nullptr;   // [G][Np] scale bits
-  uint8_t* z_r = nullptr;    // [G][Np] stored zero (zero - 1)
+  uint8_t* z_r = nullptr;    // [G][Np] stored zero field (GPTQ: zero - 1; AWQ: the zero itself)
+  int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ checkpoints, 0 for AWQ
   uint8_t* zst = nullptr;    // [Np/32][G][96]: per 32-column tile and group, 32 stored zeros then
                              // 32 scales, column c at position (c % 8) * 4 + c / 8 (small-M path)
   std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)

@@ -28,7 +28,11 @@
 //    single mask-and-or with a magic exponent, and lane t's pairs are exactly the k indices an
 //    mma.sync m16n8k16 A-fragment row needs after a fixed relabelling of k, while a whole
 //    128-row block of one column is 16*bits contiguous-by-vector bytes for the large-M loader.
-//  * s_r[g][n]: scale bits; z_r[g][n]: stored zero (zero - 1) as one byte.
+//  * s_r[g][n]: scale bits; z_r[g][n]: the checkpoint's zero field as one byte (GPTQ: zero - 1;
+//    AutoAWQ: the zero itself); the handle's zoff (1 or 0) turns the field into the zero.
+//
+// AutoAWQ GEMM checkpoints (4-bit, codes packed along the output dimension, no g_idx) go through
+// the same kernels: only the reading of a code and of a zero field differs (awq_code).
 #include "internal.cuh"
 
 #include <vector>
@@ -47,6 +51,15 @@ __device__ __forceinline__ uint32_t column_code(const int32_t* __restrict__ word
   uint32_t v = (uint32_t)__ldg(&words[row * stride]) >> sh;
   if (sh + bits > 32) v |= (uint32_t)__ldg(&words[(row + 1) * stride]) << (32 - sh);
   return v & ((1u << bits) - 1u);
+}
+
+// Code of output column n in one row of an AutoAWQ GEMM tensor (inference.shantanugoel.com ch. 39,
+// section "AWQ"): 4-bit fields packed eight to a word along the output dimension, nibble j of word
+// n / 8 holding column 8 (n / 8) + order[j] with order = 0 2 4 6 1 3 5 7.  Column o = n % 8 is
+// therefore nibble o / 2 for even o and 4 + o / 2 for odd o.
+__device__ __forceinline__ uint32_t awq_code(const int32_t* __restrict__ row, int n) {
+  const int o = n & 7;
+  return ((uint32_t)__ldg(&row[n >> 3]) >> (4 * ((o >> 1) + 4 * (o & 1)))) & 0xFu;
 }
 
 __device__ __forceinline__ int group_of(const int32_t* __restrict__ g_idx, int k, int group_size) {
@@ -156,9 +169,10 @@ __global__ void k_pads(int G, int Ks, int Kr, int last_g, const int32_t* __restr
   }
 }
 
-// One thread per (block B, vector V, column n): assembles that 16-byte vector.
+// One thread per (block B, vector V, column n): assembles that 16-byte vector.  awq: qweight is an
+// AutoAWQ [K, N/8] tensor (4-bit) instead of the GPTQ [K*bits/32, N] one.
 __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t* __restrict__ perm,
-                             int N, int Np, int bits, int nBV, uint8_t* __restrict__ wr) {
+                             int N, int Np, int bits, int nBV, int awq, uint8_t* __restrict__ wr) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= Np) return;
   for (int by = blockIdx.y; by < nBV; by += gridDim.y) {
@@ -177,7 +191,8 @@ __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t*
         const int p = jw * F + f, c = p / 4, e = 2 * (p % 4) + h;
         const int jj = 128 * B + 32 * c + 8 * t + e;
         const int k = __ldg(&perm[jj]);
-        uint32_t code = (k >= 0 && n < N) ? column_code(qweight + n, N, k, bits) : 0u;
+        uint32_t code = 0u;
+        if (k >= 0 && n < N) code = awq ? awq_code(qweight + (long)k * (N / 8), n) : column_code(qweight + n, N, k, bits);
         uint32_t val = bits == 3 ? (plane == 0 ? (code & 3u) : (code >> 2)) : code;
         word |= val << (16 * h + bp * f);
       }
@@ -188,9 +203,11 @@ __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t*
   }
 }
 
-// One thread per (group, column): scale bits and stored zero.
+// One thread per (group, column): scale bits and stored zero field (awq: qzeros is an AutoAWQ
+// [G, N/8] tensor, whose field is the zero itself).
 __global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales,
-                          int N, int Np, int bits, int G, uint16_t* __restrict__ s_r, uint8_t* __restrict__ z_r) {
+                          int N, int Np, int bits, int G, int awq, uint16_t* __restrict__ s_r,
+                          uint8_t* __restrict__ z_r) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= Np) return;
   const long wpr = (long)N * bits / 32;
@@ -199,7 +216,7 @@ __global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __
   uint8_t z = 0;
   if (n < N) {
     s = __ldg(&scales[(long)g * N + n]);
-    z = (uint8_t)column_code(qzeros + (long)g * wpr, 1, n, bits);
+    z = (uint8_t)(awq ? awq_code(qzeros + (long)g * (N / 8), n) : column_code(qzeros + (long)g * wpr, 1, n, bits));
   }
   s_r[(long)g * Np + n] = s;
   z_r[(long)g * Np + n] = z;
@@ -226,7 +243,7 @@ __global__ void k_pack_zst(const uint16_t* __restrict__ s_r, const uint8_t* __re
 }  // namespace
 
 gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, cudaStream_t st) {
+                            const int32_t* g_idx, bool awq, cudaStream_t st) {
   const int K = h.K, N = h.N, G = h.G;
   int32_t* tmp = nullptr;   // cnt[G] | off[G] | cursor[G] | meta[M_N]
   cudaError_t e = cudaMalloc(&tmp, sizeof(int32_t) * ((size_t)3 * G + M_N));
@@ -283,9 +300,10 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, h.Kr, last_g, cnt, off, h.perm, h.cgid);
   const int nBV = (h.Kr / 128) * h.bits;
   dim3 gc(h.Np / 256, nBV < 65535 ? nBV : 65535);
-  k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, h.wr);
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, awq ? 1 : 0, h.wr);
   dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
-  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, h.s_r, h.z_r);
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, awq ? 1 : 0,
+                                h.s_r, h.z_r);
   dim3 gz(h.Np / 32 / 8, G < 65535 ? G : 65535);
   k_pack_zst<<<gz, 256, 0, st>>>(h.s_r, h.z_r, h.Np, G, h.zst);
   if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
@@ -393,9 +411,9 @@ extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32
   k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, Kr, last_g, cnt, off, perm, cgid);
   const int nBV = (Kr / 128) * bits;
   dim3 gc(Np / 256, nBV < 65535 ? nBV : 65535);
-  k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, N, Np, bits, nBV, static_cast<uint8_t*>(wr));
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, N, Np, bits, nBV, 0, static_cast<uint8_t*>(wr));
   dim3 gs(Np / 256, G < 65535 ? G : 65535);
-  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, Np, bits, G,
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, Np, bits, G, 0,
                                 static_cast<uint16_t*>(s_r), z_r);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "repack launch");
   return GPTQ_OK;

@@ -32,12 +32,14 @@ _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 class GptqInfo(C.Structure):
     _fields_ = [("K", C.c_int), ("N", C.c_int), ("bits", C.c_int), ("group_size", C.c_int), ("G", C.c_int),
                 ("K_sorted", C.c_int), ("N_padded", C.c_int), ("identity", C.c_int), ("dtype", C.c_int),
-                ("reserved_M", C.c_int), ("weight_bytes", C.c_size_t), ("device_bytes", C.c_size_t)]
+                ("reserved_M", C.c_int), ("zero_offset", C.c_int), ("weight_bytes", C.c_size_t),
+                ("device_bytes", C.c_size_t)]
 
 
 SIGNATURES = {
     "gptq_check_shapes": (_I, [_I, _L, _L, _L, _L, _L, _L, _L, _I, _P, _P]),
     "gptq_repack": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "gptq_repack_awq": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "gptq_reserve": (_I, [_P, _I]),
     "gptq_gemm": (_I, [_P, _P, _P, _I, _P]),
     "gptq_gemm_path": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -148,6 +150,27 @@ def gptq_repack(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tenso
     return Handle(out.value)
 
 
+def gptq_repack_awq(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor, group_size: int,
+                    stream=None) -> Handle:
+    """AutoAWQ GEMM tensors (qweight int32 [K, N/8], qzeros int32 [G, N/8], scales [G, N], 4-bit,
+    on the current CUDA device) -> runtime handle."""
+    for name, t in (("qweight", qweight), ("qzeros", qzeros)):
+        if t.dtype != torch.int32 or t.dim() != 2 or not t.is_contiguous() or not t.is_cuda:
+            raise GptqError(1, f"{name} must be a contiguous 2-d int32 CUDA tensor")
+    if scales.dtype not in DTYPE or scales.dim() != 2 or not scales.is_contiguous() or not scales.is_cuda:
+        raise GptqError(2, "scales must be a contiguous 2-d fp16 or bf16 CUDA tensor")
+    K, N = qweight.shape[0], qweight.shape[1] * 8
+    if group_size != -1 and group_size < 1:
+        raise GptqError(1, "group_size must be -1 or >= 1")
+    G = 1 if group_size == -1 else -(-K // group_size)
+    if tuple(qzeros.shape) != (G, N // 8) or tuple(scales.shape) != (G, N):
+        raise GptqError(3, f"AWQ qweight [{K}, {N // 8}] needs qzeros [{G}, {N // 8}] and scales [{G}, {N}]")
+    out = C.c_void_p()
+    _check(lib().gptq_repack_awq(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size,
+                                 DTYPE[scales.dtype], _stream(stream), C.byref(out)))
+    return Handle(out.value)
+
+
 def gptq_reserve(h: Handle, max_M: int):
     _check(lib().gptq_reserve(h.ptr, max_M))
 
@@ -217,10 +240,17 @@ def gptq_copy_runtime(h: Handle) -> dict:
 class GptqLinear:
     """A GPTQ linear layer on the current CUDA device: repack once, then y = layer(x)."""
 
-    def __init__(self, qweight, qzeros, scales, g_idx, bits: int, group_size: int, stream=None):
-        self.handle = gptq_repack(qweight, qzeros, scales, g_idx, bits, group_size, stream)
+    def __init__(self, qweight, qzeros, scales, g_idx, bits: int, group_size: int, stream=None, *, _handle=None):
+        self.handle = _handle if _handle is not None else gptq_repack(qweight, qzeros, scales, g_idx, bits,
+                                                                        group_size, stream)
         info = gptq_get_info(self.handle)
         self.K, self.N, self.dtype = info.K, info.N, scales.dtype
+
+    @classmethod
+    def from_awq(cls, qweight, qzeros, scales, group_size: int, stream=None) -> "GptqLinear":
+        """The same layer object built from an AutoAWQ GEMM checkpoint."""
+        return cls(None, None, scales, None, 4, group_size, _handle=gptq_repack_awq(qweight, qzeros, scales,
+                                                                                    group_size, stream))
 
     def __call__(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         if x.dtype != self.dtype or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
