@@ -8,5 +8,5 @@ it with ctypes and numpy.
 from .oracle import (  # noqa: F401
     build, lib, unpack_codes, pack_codes, unpack_zeros, pack_zeros, num_groups,
     dequant, linear, check_rules, runtime_dims, runtime_layout, num_threads, half_to_float,
-    awq_unpack, awq_pack, awq_dequant, awq_linear, awq_to_gptq_fields,
+    awq_unpack, awq_pack, awq_dequant, awq_linear, awq_to_gptq_fields, round_fp32,
 )

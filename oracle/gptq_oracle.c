@@ -76,6 +76,54 @@ static float half_bits_to_float(uint16_t h, int dtype) {
 
 float oracle_half_to_float(uint16_t h, int dtype) { return half_bits_to_float(h, dtype); }
 
+/*
+ * float32 -> binary16 / bfloat16 bits, round to nearest, ties to even (IEEE 754), written from the
+ * formats' definitions with integers only.  Used where the library takes float32 scales ([P5]
+ * GptqLayer: scales are float16 "or the layer weight dtype"; its Example file stores F32 scales):
+ * a layer that computes in fp16/bf16 uses its scales in that type, so they are rounded once.
+ *   value = S * 2^E exactly (S the 24-bit significand); the target keeps mb fraction bits, its
+ *   smallest quantum is 2^qmin (qmin = 1 - bias - mb, the subnormal spacing), and a value whose
+ *   rounded exponent field reaches all ones is infinity.
+ */
+static uint16_t round_fp32_bits(uint32_t u, int mb, int eb, int bias) {
+  const uint32_t sign = (u >> 31) << (mb + eb);
+  const uint32_t expo = (u >> 23) & 0xFFu, frac = u & 0x7FFFFFu;
+  const uint32_t inf = ((1u << eb) - 1u) << mb;
+  if (expo == 0xFFu) return (uint16_t)(sign | inf | (frac ? 1u << (mb - 1) : 0u));   /* nan / inf */
+  uint64_t S = expo ? (frac | 0x800000u) : frac;
+  int E = expo ? (int)expo - 127 - 23 : -149;
+  if (S == 0) return (uint16_t)sign;
+  int top = 63;
+  while (!((S >> top) & 1u)) --top;                    /* floor(log2 S) */
+  const int qmin = 1 - bias - mb;
+  int q = top + E - mb;                                 /* quantum that keeps mb fraction bits */
+  if (q < qmin) q = qmin;
+  uint64_t m;
+  const int shift = q - E;
+  if (shift <= 0) {
+    m = S << -shift;
+  } else if (shift > 40) {
+    m = 0;                                              /* below half the smallest quantum */
+  } else {
+    m = S >> shift;
+    const uint64_t rem = S & ((1ull << shift) - 1u), half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (m & 1u))) ++m;
+  }
+  if (m >> (mb + 1)) { m >>= 1; ++q; }                  /* rounding carried into a new binade */
+  if (m < (1ull << mb)) return (uint16_t)(sign | (uint32_t)m);   /* subnormal (q == qmin) or zero */
+  const int biased = q + mb + bias;
+  if (biased >= (1 << eb) - 1) return (uint16_t)(sign | inf);
+  return (uint16_t)(sign | ((uint32_t)biased << mb) | (uint32_t)(m - (1ull << mb)));
+}
+
+/* n float32 values (as bits) -> dtype bits: DT_FP16 binary16, DT_BF16 bfloat16. */
+int oracle_round_fp32(const uint32_t* in, long n, int dtype, uint16_t* out) {
+  if (dtype != DT_FP16 && dtype != DT_BF16) return 1;
+  for (long i = 0; i < n; ++i)
+    out[i] = dtype == DT_FP16 ? round_fp32_bits(in[i], 10, 5, 15) : round_fp32_bits(in[i], 7, 8, 127);
+  return 0;
+}
+
 /* ---- unpacking codes along one axis ---- */
 
 /*
@@ -180,15 +228,19 @@ static int group_of(const int32_t* g_idx, long k, int group_size) {
 
 /*
  * One dequantised weight row n (all K inputs), float32, per the Reader:
- *   W[n, k] = (float(code[k, n]) - float(z[g, n])) * float(scales[g, n]),  g = g_idx[k].
+ *   W[n, k] = (float(code[k, n]) - float(z[g, n])) * float(scales[g, n]),  g = g_idx[k],
+ * z = stored field + zoff: zoff 1 for the AutoGPTQ (v1) fields stored minus one ([P4] "The
+ * format"), 0 for the corrected gptq_v2 fields that hold the zero itself (same section; [P1]
+ * keeps the v1/v2 interpretation apart).
  */
 static void dequant_row(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
-                        const int32_t* g_idx, int K, int N, int bits, int group_size, long n, float* row) {
+                        const int32_t* g_idx, int K, int N, int bits, int group_size, uint32_t zoff, long n,
+                        float* row) {
   long wpr = (long)N * bits / 32;
   for (long k = 0; k < K; ++k) {
     int g = group_of(g_idx, k, group_size);
     float q = (float)code_at(qweight + n, N, k, bits);
-    float z = (float)(code_at(qzeros + (long)g * wpr, 1, n, bits) + 1u);
+    float z = (float)(code_at(qzeros + (long)g * wpr, 1, n, bits) + zoff);
     float s = half_bits_to_float(scales[(long)g * N + n], dtype);
     row[k] = (q - z) * s;
   }
@@ -201,29 +253,39 @@ static int check_gidx(const int32_t* g_idx, int K, int G) {
   return ORACLE_OK;
 }
 
-/* Dense W float32 [N][K] (the Reader's output, [out_features, in_features]). */
-int oracle_dequant(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
-                   const int32_t* g_idx, int K, int N, int bits, int group_size, float* W) {
+/* Dense W float32 [N][K] (the Reader's output, [out_features, in_features]); zoff as dequant_row. */
+int oracle_dequant_ex(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                      const int32_t* g_idx, int K, int N, int bits, int group_size, int zoff, float* W) {
   int G = oracle_num_groups(K, group_size);
   if (!bits_ok(bits) || K % 32 || N % 32 || G <= 0 || check_gidx(g_idx, K, G)) return ORACLE_EINVAL;
   if (!g_idx && group_size != -1 && group_size > K) return ORACLE_EINVAL;
+  if (zoff != 0 && zoff != 1) return ORACLE_EINVAL;
 #pragma omp parallel for schedule(static)
   for (long n = 0; n < N; ++n)
-    dequant_row(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, n, W + n * (long)K);
+    dequant_row(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, (uint32_t)zoff, n, W + n * (long)K);
   return ORACLE_OK;
 }
 
+int oracle_dequant(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                   const int32_t* g_idx, int K, int N, int bits, int group_size, float* W) {
+  return oracle_dequant_ex(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, 1, W);
+}
+
 /*
- * y[r][c] = sum_k x[rows[r]][k] * W[cols[c]][k], over the sampled rows and columns.
+ * y[r][c] = sum_k x[rows[r]][k] * W[cols[c]][k] (+ bias[cols[c]]), over the sampled rows and columns.
  * x: [M][K] fp16/bf16 bits.  The weight row W[n] is dequantised once per sampled column, then
- * dotted with each sampled x row in ascending k, accumulating in double.
+ * dotted with each sampled x row in ascending k, accumulating in double; the bias ([P5]
+ * GptqLayer: optional, [out_features], same dtype as scales) is added to the double sum.
+ * zoff as dequant_row.  bias: NULL, or N values of bias_kind 0 (fp16 bits), 1 (bf16 bits) or
+ * 2 (float32).
  */
-int oracle_linear(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
-                  const int32_t* g_idx, int K, int N, int bits, int group_size,
-                  const uint16_t* x, int M, const int32_t* rows, int nrows, const int32_t* cols, int ncols,
-                  double* y) {
+int oracle_linear_ex(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                     const int32_t* g_idx, int K, int N, int bits, int group_size, int zoff, const void* bias,
+                     int bias_kind, const uint16_t* x, int M, const int32_t* rows, int nrows, const int32_t* cols,
+                     int ncols, double* y) {
   int G = oracle_num_groups(K, group_size);
   if (!bits_ok(bits) || K % 32 || N % 32 || G <= 0 || check_gidx(g_idx, K, G)) return ORACLE_EINVAL;
+  if ((zoff != 0 && zoff != 1) || bias_kind < 0 || bias_kind > 2) return ORACLE_EINVAL;
   for (int r = 0; r < nrows; ++r) if (rows[r] < 0 || rows[r] >= M) return ORACLE_EINVAL;
   for (int c = 0; c < ncols; ++c) if (cols[c] < 0 || cols[c] >= N) return ORACLE_EINVAL;
   float* xf = (float*)malloc(sizeof(float) * (size_t)nrows * K);
@@ -240,12 +302,18 @@ int oracle_linear(const int32_t* qweight, const int32_t* qzeros, const uint16_t*
     } else {
 #pragma omp for schedule(static)
       for (long c = 0; c < ncols; ++c) {
-        dequant_row(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, cols[c], row);
+        dequant_row(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, (uint32_t)zoff, cols[c], row);
+        double b = 0.0;
+        if (bias) {
+          const long n = cols[c];
+          b = bias_kind == 2 ? (double)((const float*)bias)[n]
+                             : (double)half_bits_to_float(((const uint16_t*)bias)[n], bias_kind == 1 ? DT_BF16 : DT_FP16);
+        }
         for (long r = 0; r < nrows; ++r) {
           double acc = 0.0;
           const float* xr = xf + r * K;
           for (long k = 0; k < K; ++k) acc += (double)xr[k] * (double)row[k];
-          y[r * ncols + c] = acc;
+          y[r * ncols + c] = bias ? acc + b : acc;
         }
       }
       free(row);
@@ -253,6 +321,14 @@ int oracle_linear(const int32_t* qweight, const int32_t* qzeros, const uint16_t*
   }
   free(xf);
   return fail ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+int oracle_linear(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales, int dtype,
+                  const int32_t* g_idx, int K, int N, int bits, int group_size,
+                  const uint16_t* x, int M, const int32_t* rows, int nrows, const int32_t* cols, int ncols,
+                  double* y) {
+  return oracle_linear_ex(qweight, qzeros, scales, dtype, g_idx, K, N, bits, group_size, 1, NULL, 0, x, M, rows,
+                          nrows, cols, ncols, y);
 }
 
 /* Thread count the parallel loops above use (1 when built without OpenMP). */

@@ -53,6 +53,9 @@ def lib():
                 "oracle_num_groups": [I, I],
                 "oracle_dequant": [P, P, P, I, P, I, I, I, I, P],
                 "oracle_linear": [P, P, P, I, P, I, I, I, I, P, I, P, I, P, I, P],
+                "oracle_dequant_ex": [P, P, P, I, P, I, I, I, I, I, P],
+                "oracle_linear_ex": [P, P, P, I, P, I, I, I, I, I, P, I, P, I, P, I, P, I, P],
+                "oracle_round_fp32": [P, C.c_long, I, P],
                 "oracle_check_rules": [I, I, I, I, I, I, I, I, P, I],
                 "oracle_runtime_dims": [P, I, I, I, P, P],
                 "oracle_runtime_layout": [P, P, P, P, I, I, I, I, P, P, P, P, P],
@@ -137,20 +140,28 @@ def pack_zeros(z, bits: int) -> np.ndarray:
     return out
 
 
-def dequant(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: str) -> np.ndarray:
-    """Dense W float32 [N, K]."""
+def dequant(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: str,
+            zero_offset: int = 1) -> np.ndarray:
+    """Dense W float32 [N, K].  zero_offset: 1 for v1 zero fields (stored minus one), 0 for gptq_v2."""
     qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
     sc, gi = _np(scales, np.uint16), _np(g_idx, np.int32)
     K, N = qw.shape[0] * 32 // bits, qw.shape[1]
     W = np.empty((N, K), np.float32)
-    _check(lib().oracle_dequant(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size, _p(W)),
-           "dequant")
+    if zero_offset == 1:
+        _check(lib().oracle_dequant(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size, _p(W)),
+               "dequant")
+    else:
+        _check(lib().oracle_dequant_ex(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size,
+                                       zero_offset, _p(W)), "dequant_ex")
     return W
 
 
 def linear(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: str, x,
-           rows=None, cols=None) -> np.ndarray:
-    """y[rows][cols] = x[rows] . W[cols]^T in float64 (all rows / columns by default)."""
+           rows=None, cols=None, zero_offset: int = 1, bias=None) -> np.ndarray:
+    """y[rows][cols] = x[rows] . W[cols]^T (+ bias[cols]) in float64 (all rows / columns by default).
+
+    zero_offset: 1 for v1 zero fields (stored minus one), 0 for gptq_v2.  bias: None, or [N]
+    float16 / bfloat16 / float32 (a torch tensor or a numpy float16/float32 array)."""
     qw, qz = _np(qweight, np.int32), _np(qzeros, np.int32)
     sc, gi = _np(scales, np.uint16), _np(g_idx, np.int32)
     xx = _np(x, np.uint16)
@@ -160,9 +171,45 @@ def linear(qweight, qzeros, scales, g_idx, bits: int, group_size: int, dtype: st
     r = np.arange(M, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
     c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, np.int32)
     y = np.empty((len(r), len(c)), np.float64)
-    _check(lib().oracle_linear(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size,
-                               _p(xx), M, _p(r), len(r), _p(c), len(c), _p(y)), "linear")
+    if zero_offset == 1 and bias is None:
+        _check(lib().oracle_linear(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size,
+                                   _p(xx), M, _p(r), len(r), _p(c), len(c), _p(y)), "linear")
+        return y
+    b, kind = _bias(bias, N)
+    _check(lib().oracle_linear_ex(_p(qw), _p(qz), _p(sc), DT[dtype], _p(gi), K, N, bits, group_size, zero_offset,
+                                  _p(b), kind, _p(xx), M, _p(r), len(r), _p(c), len(c), _p(y)), "linear_ex")
     return y
+
+
+def _bias(bias, N):
+    """(array, kind) for oracle_linear_ex: kind 0 fp16 bits, 1 bf16 bits, 2 float32."""
+    if bias is None:
+        return None, 0
+    import torch
+    if isinstance(bias, torch.Tensor):
+        t = bias.detach().cpu().contiguous()
+        assert t.numel() == N
+        if t.dtype == torch.float32:
+            return t.numpy(), 2
+        kind = {torch.float16: 0, torch.bfloat16: 1}[t.dtype]
+        return t.view(torch.int16).numpy().view(np.uint16), kind
+    a = np.ascontiguousarray(bias)
+    assert a.size == N
+    if a.dtype == np.float32:
+        return a, 2
+    assert a.dtype == np.float16
+    return a.view(np.uint16), 0
+
+
+def round_fp32(values, dtype: str) -> np.ndarray:
+    """float32 values -> fp16 / bf16 bits (uint16), round to nearest even."""
+    import torch
+    if isinstance(values, torch.Tensor):
+        values = values.detach().cpu().contiguous().numpy()
+    v = np.ascontiguousarray(values, np.float32)
+    out = np.empty(v.shape, np.uint16)
+    _check(lib().oracle_round_fp32(_p(v.view(np.uint32)), v.size, DT[dtype], _p(out)), "round_fp32")
+    return out
 
 
 def check_rules(bits, qweight_shape, qzeros_shape, scales_shape, in_features, g_idx=None) -> int:
