@@ -390,10 +390,41 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
     one("llama3-70b-gate-8192x28672-b4g128-descact", s3, m3, 4)
     s4, m4 = synth.workload("prefill-8192x28672-b4g128")
     one("prefill-8192x28672-b4g128", s4, [4096] if args.quick_prefill else m4, 1)
+    out["awq-4096x14336-b4g128-fp16"] = awq_layer(hbm, tf_burst)
     if not args.no_sweep:
         out["format-sweep-4096x4096"] = format_sweep(hbm, tf_burst)
     out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "kind": peak_kind}
     return out
+
+
+def awq_layer(hbm, tf_burst):
+    """An AutoAWQ GEMM checkpoint of the decode layer's shape (K = 4096, N = 14336, 4-bit, group
+    128, fp16, asymmetric zeros) through gptq_repack_awq, at M = 1, 16 and 512; 16 handles
+    rotated so every call streams its weights from HBM."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    K, N, gs = 4096, 14336, 128
+    spec = synth.LayerSpec(K, N, 4, gs, False, False, "fp16")     # for the byte count only
+    ck = synth.make_awq_checkpoint(K, N, gs, "fp16", seed=5)
+    dev = [ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda()]
+    hs = [gptq.gptq_repack_awq(dev[0], dev[1], dev[2], gs) for _ in range(LAYERS)]
+    torch.cuda.synchronize()
+    r = {"layers_rotated": LAYERS}
+    for M in (1, 16, 512):
+        xs = [synth.make_x(M, K, "fp16", seed=M + i).cuda() for i in range(4)]
+        ys = [torch.empty(M, N, dtype=torch.float16, device="cuda") for _ in range(4)]
+        t = time_calls(hs, xs, ys, M, 200 if M <= 64 else 50, 3, graph=True)
+        B, F = b_alg(spec, M), 2.0 * M * N * K
+        roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
+        r[f"M={M}"] = {"us": round(t * 1e6, 2), "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),
+                       "roofline_frac": round(roof / t, 4),
+                       "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+        del xs, ys
+    for h in hs:
+        h.close()
+    del hs, dev
+    torch.cuda.empty_cache()
+    return r
 
 
 def format_sweep(hbm, tf_burst):

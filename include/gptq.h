@@ -113,6 +113,41 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
  */
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
 
+/* Flags of gptq_repack_ex. */
+#define GPTQ_REPACK_ZEROS_V2    1u  /* qzeros fields hold the zero itself (the corrected gptq_v2
+                                       layout named in ch. 39, "The format"), not zero - 1      */
+#define GPTQ_REPACK_SCALES_FP32 2u  /* scales are float32 [G, N] (tensref.org GptqLayer allows the
+                                       layer weight dtype; its Example stores F32): they are
+                                       rounded once to `dtype`, to nearest even, at repack       */
+
+/*
+ * gptq_repack with format options.  flags = 0 is exactly gptq_repack.
+ *   GPTQ_REPACK_ZEROS_V2     W[n, k] = (code - field) * scale; gptq_get_info reports
+ *                            zero_offset = 0.  Fields 0 .. 2^bits - 1 are all valid zeros.
+ *   GPTQ_REPACK_SCALES_FP32  `scales` is device float32 [G, N], 4-byte aligned; the kernels use
+ *                            the rounded value, so y differs from a float32-scale product by at
+ *                            most the scale rounding (2^-11 relative for fp16, 2^-9 for bf16,
+ *                            per group).
+ * Other arguments and errors as gptq_repack (INVALID_ARG also for unknown flag bits).
+ */
+gptq_status_t gptq_repack_ex(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                             const int32_t* g_idx, int K, int N, int bits, int group_size,
+                             gptq_dtype_t dtype, unsigned flags, void* stream, gptq_handle_t* out);
+
+/*
+ * Attach the layer's bias (tensref.org GptqLayer: optional, [out_features], same dtype as the
+ * scales): every later gptq_gemm / gptq_gemm_path on this handle computes y = x . W^T + bias,
+ * the bias added in fp32 before the single rounding of y.
+ *   bias       device, [N] of the handle's dtype (bias_fp32 = 0) or float32 (bias_fp32 = 1),
+ *              2- or 4-byte aligned; copied (as float32) on `stream`, so it may be freed once
+ *              that stream has passed this call.  NULL detaches the bias.
+ * The first non-NULL call allocates N_padded float32 on the device; later calls reuse it.  Calls
+ * captured in a CUDA graph before the first attach keep running without a bias.  Must not run
+ * while a gptq_gemm on the handle is in flight on another stream.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+gptq_status_t gptq_set_bias(gptq_handle_t h, const void* bias, int bias_fp32, void* stream);
+
 /*
  * Build a runtime handle from one AutoAWQ GEMM layer (inference.shantanugoel.com ch. 39
  * "Quantized checkpoints", section "AWQ": the pack_awq / unpack_awq / from_checkpoint
@@ -170,7 +205,8 @@ typedef struct {
   int identity;     /* 1 when the sorted order is k itself (no permutation, no padding)       */
   gptq_dtype_t dtype;
   int reserved_M;   /* largest M gptq_gemm accepts on every path without further reserve      */
-  int zero_offset;  /* zero = stored zero field + zero_offset: 1 (gptq_repack), 0 (gptq_repack_awq) */
+  int zero_offset;  /* zero = stored zero field + zero_offset: 1 (GPTQ v1), 0 (gptq_v2, AWQ)     */
+  int has_bias;     /* 1 while a bias is attached (gptq_set_bias)                              */
   size_t weight_bytes;     /* runtime codes: K_sorted/128 * bits * N_padded * 16              */
   size_t device_bytes;     /* everything the handle holds on the device                      */
 } gptq_info_t;

@@ -31,7 +31,7 @@ gptq_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, bool awq, cudaStream_t st);
+                            const int32_t* g_idx, bool awq, bool scales_fp32, cudaStream_t st);
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -44,6 +44,7 @@ static void free_handle(Handle* h) {
   cudaFree(h->z_r);
   cudaFree(h->zst);
   cudaFree(h->xp);
+  cudaFree(h->bias);
   cudaFree(h->err);
   delete h;
 }
@@ -165,7 +166,7 @@ namespace gptq {
 // Argument checks shared by both checkpoint formats, then the handle and its runtime layout.
 static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, const void* scales,
                                  const int32_t* g_idx, int K, int N, int bits, int group_size, gptq_dtype_t dtype,
-                                 bool awq, void* stream, gptq_handle_t* out) {
+                                 bool awq, unsigned flags, void* stream, gptq_handle_t* out) {
   if (!out) return fail(GPTQ_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!qweight || !qzeros || !scales) return fail(GPTQ_ERR_INVALID_ARG, "qweight, qzeros and scales are required");
@@ -179,8 +180,11 @@ static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, 
   const int G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
   if (K > kMaxK || N > kMaxN || G > kMaxGroups)
     return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= 131072, N <= 262144, groups <= 65536)");
-  if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, 2) || (g_idx && !aligned(g_idx, 4)))
-    return fail(GPTQ_ERR_ALIGNMENT, "qweight, qzeros, g_idx need 4-byte and scales 2-byte alignment");
+  if (flags & ~(unsigned)(GPTQ_REPACK_ZEROS_V2 | GPTQ_REPACK_SCALES_FP32))
+    return fail(GPTQ_ERR_INVALID_ARG, "unknown repack flag bits");
+  const bool sf32 = (flags & GPTQ_REPACK_SCALES_FP32) != 0;
+  if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, sf32 ? 4 : 2) || (g_idx && !aligned(g_idx, 4)))
+    return fail(GPTQ_ERR_ALIGNMENT, "qweight, qzeros, g_idx need 4-byte and scales 2-byte (float32: 4-byte) alignment");
   int dev = 0, sms = 0;
   gptq_status_t s = check_device(&dev, &sms);
   if (s != GPTQ_OK) return s;
@@ -191,11 +195,11 @@ static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, 
   h->K = K; h->N = N; h->bits = bits; h->group_size = group_size; h->G = G;
   h->Np = (N + 255) / 256 * 256;
   h->dtype = dtype;
-  h->zoff = awq ? 0 : 1;
+  h->zoff = (awq || (flags & GPTQ_REPACK_ZEROS_V2)) ? 0 : 1;
   cudaError_t ce = cudaMalloc(&h->err, sizeof(int32_t));
   if (ce == cudaSuccess) ce = cudaMemsetAsync(h->err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaMalloc(error word)"); }
-  s = build_runtime(*h, qweight, qzeros, scales, g_idx, awq, static_cast<cudaStream_t>(stream));
+  s = build_runtime(*h, qweight, qzeros, scales, g_idx, awq, sf32, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
   s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 32);
@@ -210,12 +214,44 @@ extern "C" {
 gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
                           int K, int N, int bits, int group_size, gptq_dtype_t dtype, void* stream,
                           gptq_handle_t* out) {
-  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, stream, out);
+  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, 0u, stream, out);
+}
+
+gptq_status_t gptq_repack_ex(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
+                             int K, int N, int bits, int group_size, gptq_dtype_t dtype, unsigned flags, void* stream,
+                             gptq_handle_t* out) {
+  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, flags, stream, out);
+}
+
+gptq_status_t gptq_set_bias(gptq_handle_t hh, const void* bias, int bias_fp32, void* stream) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  Handle& h = *reinterpret_cast<Handle*>(hh);
+  if (bias_fp32 != 0 && bias_fp32 != 1) return fail(GPTQ_ERR_INVALID_ARG, "bias_fp32 must be 0 or 1");
+  if (!bias) {
+    h.has_bias = 0;
+    return GPTQ_OK;
+  }
+  if (!aligned(bias, bias_fp32 ? 4 : 2)) return fail(GPTQ_ERR_ALIGNMENT, "bias needs 2-byte (float32: 4-byte) alignment");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h.device)
+    return fail(GPTQ_ERR_INVALID_ARG, "handle belongs to device " + std::to_string(h.device) + " but device " +
+                                          std::to_string(dev) + " is current");
+  if (!h.bias && (e = cudaMalloc(&h.bias, sizeof(float) * (size_t)h.Np)) != cudaSuccess) {
+    h.bias = nullptr;
+    return cuda_fail(e, "cudaMalloc(bias)");
+  }
+  const int kind = bias_fp32 ? 2 : (h.dtype == GPTQ_BF16 ? 1 : 0);
+  if ((e = launch_bias_f32(bias, kind, h.N, h.Np, h.bias, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "bias conversion launch");
+  h.has_bias = 1;
+  return GPTQ_OK;
 }
 
 gptq_status_t gptq_repack_awq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int K, int N,
                               int group_size, gptq_dtype_t dtype, void* stream, gptq_handle_t* out) {
-  return repack_impl(qweight, qzeros, scales, nullptr, K, N, 4, group_size, dtype, true, stream, out);
+  return repack_impl(qweight, qzeros, scales, nullptr, K, N, 4, group_size, dtype, true, 0u, stream, out);
 }
 
 gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
@@ -286,9 +322,10 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->K_sorted = h.Kr; info->N_padded = h.Np; info->identity = h.identity; info->dtype = h.dtype;
   info->reserved_M = h.reserved_M;
   info->zero_offset = h.zoff;
+  info->has_bias = h.has_bias;
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
-                       (size_t)h.G * h.Np * 6 + h.xp_bytes;
+                       (size_t)h.G * h.Np * 6 + h.xp_bytes + (h.bias ? sizeof(float) * (size_t)h.Np : 0);
   return GPTQ_OK;
 }
 

@@ -91,7 +91,8 @@ struct LargeArgs {
   const uint8_t* wr; const int32_t* cgid; const uint16_t* s_r; const uint8_t* z_r;
   void* y; int32_t* err;
   int M, N, Np, Kr, G;
-  int zoff;         // zero = stored byte + zoff (1: GPTQ fields; 0: AWQ fields)
+  int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields; 0: gptq_v2, AWQ)
+  const float* bias;   // [Np] float32 added to y, or nullptr
 };
 
 __device__ __forceinline__ uint32_t and_or_l(uint32_t a, uint32_t b, uint32_t c) {
@@ -385,6 +386,11 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     // y[m][n] for the HC x rows of this half: lanes are consecutive n, so each store is 64 bytes
     uint16_t* y = static_cast<uint16_t*>(a.y);
     if (n < a.N) {
+      if (a.bias) {
+        const float b = __ldg(a.bias + n);
+#pragma unroll
+        for (int j = 0; j < HC; ++j) acc[j] += b;
+      }
 #pragma unroll
       for (int j = 0; j < HC; ++j) {
         const int m = m0 + HC * hs + j;
@@ -570,7 +576,7 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff};
+  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff, h.has_bias ? h.bias : nullptr};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, 1);     // consecutive CTAs share a weight tile
   cfg.blockDim = dim3(kThreadsL);

@@ -264,7 +264,8 @@ struct SmallArgs {
   int o_raw;        // the caller's x rows, [M][K] as given
   int cg_async;     // 1: the producer bulk-copies the chunk-group table (CTAs that own a whole SM, whose
                     // start is not hidden behind the previous call); 0: every thread loads it at start
-  int zoff;         // zero = stored byte + zoff (1: GPTQ fields, stored minus one; 0: AWQ fields)
+  int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields, stored minus one; 0: gptq_v2, AWQ)
+  const float* bias;   // [Np] float32 added to y, or nullptr
 };
 
 template <int CW>
@@ -683,6 +684,10 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       }
       const int n = ti * kTileN + cl;
       if (n < a.N) {   // N % 32 == 0: a group of 4 columns is all in or all out
+        if (a.bias) {
+          const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + n));
+          sum.x += b.x; sum.y += b.y; sum.z += b.z; sum.w += b.w;
+        }
         uint2 o;
         o.x = pack2<T>(sum.x, sum.y);
         o.y = pack2<T>(sum.z, sum.w);
@@ -828,7 +833,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
-                 h.zoff};
+                 h.zoff, h.has_bias ? h.bias : nullptr};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());

@@ -31,7 +31,9 @@ struct Handle {
   int32_t* cgid = nullptr;   // [Kr/32] group of each 32-row chunk
   uint16_t* s_r = nullptr;   // [G][Np] scale bits
   uint8_t* z_r = nullptr;    // [G][Np] stored zero field (GPTQ: zero - 1; AWQ: the zero itself)
-  int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ checkpoints, 0 for AWQ
+  int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ v1 fields, 0 for gptq_v2 and AWQ
+  float* bias = nullptr;     // [Np] float32 bias added to y (pad columns 0), allocated by gptq_set_bias
+  int has_bias = 0;          // 1: the GEMM kernels add bias
   uint8_t* zst = nullptr;    // [Np/32][G][96]: per 32-column tile and group, 32 stored zeros then
                              // 32 scales, column c at position (c % 8) * 4 + c / 8 (small-M path)
   std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)
@@ -73,6 +75,9 @@ gptq_status_t fail(gptq_status_t s, const std::string& msg);
 gptq_status_t cuda_fail(cudaError_t e, const char* what);
 
 // ---- kernels launched from the host code (defined in the .cu files) ----
+
+// bias[n] -> float32 [Np] (kind 0 fp16, 1 bf16, 2 float32; pad columns 0), enqueued on st.
+cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst, cudaStream_t st);
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);

@@ -204,10 +204,11 @@ __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t*
 }
 
 // One thread per (group, column): scale bits and stored zero field (awq: qzeros is an AutoAWQ
-// [G, N/8] tensor, whose field is the zero itself).
-__global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __restrict__ scales,
-                          int N, int Np, int bits, int G, int awq, uint16_t* __restrict__ s_r,
-                          uint8_t* __restrict__ z_r) {
+// [G, N/8] tensor, whose field is the zero itself).  sf32: scales are float32, rounded here to the
+// handle's dtype (round to nearest even; bf16 when to_bf16) -- the type the layer computes in.
+__global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const void* __restrict__ scales,
+                          int N, int Np, int bits, int G, int awq, int sf32, int to_bf16,
+                          uint16_t* __restrict__ s_r, uint8_t* __restrict__ z_r) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= Np) return;
   const long wpr = (long)N * bits / 32;
@@ -215,7 +216,12 @@ __global__ void k_pack_sz(const int32_t* __restrict__ qzeros, const uint16_t* __
   uint16_t s = 0;
   uint8_t z = 0;
   if (n < N) {
-    s = __ldg(&scales[(long)g * N + n]);
+    if (sf32) {
+      const float f = __ldg(static_cast<const float*>(scales) + (long)g * N + n);
+      s = to_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f)) : __half_as_ushort(__float2half_rn(f));
+    } else {
+      s = __ldg(static_cast<const uint16_t*>(scales) + (long)g * N + n);
+    }
     z = (uint8_t)(awq ? awq_code(qzeros + (long)g * (N / 8), n) : column_code(qzeros + (long)g * wpr, 1, n, bits));
   }
   s_r[(long)g * Np + n] = s;
@@ -240,10 +246,30 @@ __global__ void k_pack_zst(const uint16_t* __restrict__ s_r, const uint8_t* __re
   }
 }
 
+// bias[n] as float32 (0 for the pad columns n >= N): kind 0 fp16 bits, 1 bf16 bits, 2 float32.
+__global__ void k_bias_f32(const void* __restrict__ src, int kind, int N, int Np, float* __restrict__ dst) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= Np) return;
+  float v = 0.0f;
+  if (n < N) {
+    if (kind == 2) v = __ldg(static_cast<const float*>(src) + n);
+    else {
+      const uint16_t b = __ldg(static_cast<const uint16_t*>(src) + n);
+      v = kind == 1 ? __bfloat162float(__ushort_as_bfloat16(b)) : __half2float(__ushort_as_half(b));
+    }
+  }
+  dst[n] = v;
+}
+
 }  // namespace
 
+cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst, cudaStream_t st) {
+  k_bias_f32<<<(Np + 255) / 256, 256, 0, st>>>(src, kind, N, Np, dst);
+  return cudaGetLastError();
+}
+
 gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, bool awq, cudaStream_t st) {
+                            const int32_t* g_idx, bool awq, bool scales_fp32, cudaStream_t st) {
   const int K = h.K, N = h.N, G = h.G;
   int32_t* tmp = nullptr;   // cnt[G] | off[G] | cursor[G] | meta[M_N]
   cudaError_t e = cudaMalloc(&tmp, sizeof(int32_t) * ((size_t)3 * G + M_N));
@@ -302,8 +328,8 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   dim3 gc(h.Np / 256, nBV < 65535 ? nBV : 65535);
   k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, awq ? 1 : 0, h.wr);
   dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
-  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, h.Np, h.bits, G, awq ? 1 : 0,
-                                h.s_r, h.z_r);
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, scales, N, h.Np, h.bits, G, awq ? 1 : 0, scales_fp32 ? 1 : 0,
+                                h.dtype == GPTQ_BF16 ? 1 : 0, h.s_r, h.z_r);
   dim3 gz(h.Np / 32 / 8, G < 65535 ? G : 65535);
   k_pack_zst<<<gz, 256, 0, st>>>(h.s_r, h.z_r, h.Np, G, h.zst);
   if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
@@ -413,8 +439,7 @@ extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32
   dim3 gc(Np / 256, nBV < 65535 ? nBV : 65535);
   k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, N, Np, bits, nBV, 0, static_cast<uint8_t*>(wr));
   dim3 gs(Np / 256, G < 65535 ? G : 65535);
-  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, static_cast<const uint16_t*>(scales), N, Np, bits, G, 0,
-                                static_cast<uint16_t*>(s_r), z_r);
+  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, scales, N, Np, bits, G, 0, 0, 0, static_cast<uint16_t*>(s_r), z_r);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "repack launch");
   return GPTQ_OK;
 }

@@ -21,6 +21,7 @@ STATUS = {0: "GPTQ_OK", 1: "GPTQ_ERR_INVALID_ARG", 2: "GPTQ_ERR_UNSUPPORTED", 3:
           8: "GPTQ_ERR_DEVICE", 9: "GPTQ_ERR_TIMEOUT"}
 PATH_AUTO, PATH_SMALL_M, PATH_LARGE_M = 0, 1, 2
 DTYPE = {torch.float16: 0, torch.bfloat16: 1}
+REPACK_ZEROS_V2, REPACK_SCALES_FP32 = 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -32,7 +33,7 @@ _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 class GptqInfo(C.Structure):
     _fields_ = [("K", C.c_int), ("N", C.c_int), ("bits", C.c_int), ("group_size", C.c_int), ("G", C.c_int),
                 ("K_sorted", C.c_int), ("N_padded", C.c_int), ("identity", C.c_int), ("dtype", C.c_int),
-                ("reserved_M", C.c_int), ("zero_offset", C.c_int), ("weight_bytes", C.c_size_t),
+                ("reserved_M", C.c_int), ("zero_offset", C.c_int), ("has_bias", C.c_int), ("weight_bytes", C.c_size_t),
                 ("device_bytes", C.c_size_t)]
 
 
@@ -40,6 +41,8 @@ SIGNATURES = {
     "gptq_check_shapes": (_I, [_I, _L, _L, _L, _L, _L, _L, _L, _I, _P, _P]),
     "gptq_repack": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "gptq_repack_awq": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "gptq_repack_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, C.c_uint, _P, _P]),
+    "gptq_set_bias": (_I, [_P, _P, _I, _P]),
     "gptq_reserve": (_I, [_P, _I]),
     "gptq_gemm": (_I, [_P, _P, _P, _I, _P]),
     "gptq_gemm_path": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -133,21 +136,54 @@ class Handle:
 
 
 def gptq_repack(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor, g_idx: Optional[torch.Tensor],
-                bits: int, group_size: int, stream=None) -> Handle:
-    """Checkpoint tensors (on the current CUDA device) -> runtime handle."""
+                bits: int, group_size: int, stream=None, *, zeros_v2: bool = False,
+                dtype: Optional[torch.dtype] = None) -> Handle:
+    """Checkpoint tensors (on the current CUDA device) -> runtime handle.
+
+    zeros_v2: the qzeros fields hold the zero itself (gptq_v2) instead of zero - 1.  Float32
+    scales are accepted with `dtype` (float16 / bfloat16) naming the layer's compute type; they are
+    rounded to it once.  Either option goes through gptq_repack_ex."""
     K, N = gptq_check_shapes(bits, tuple(qweight.shape), tuple(qzeros.shape), tuple(scales.shape),
                              0 if g_idx is None else g_idx.numel(), group_size)
     for name, t, dt in (("qweight", qweight, torch.int32), ("qzeros", qzeros, torch.int32)):
         if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
             raise GptqError(1, f"{name} must be a contiguous int32 CUDA tensor")
-    if scales.dtype not in DTYPE or not scales.is_contiguous() or not scales.is_cuda:
-        raise GptqError(2, "scales must be a contiguous fp16 or bf16 CUDA tensor")
+    if scales.dtype not in (torch.float16, torch.bfloat16, torch.float32) or not scales.is_contiguous() \
+            or not scales.is_cuda:
+        raise GptqError(2, "scales must be a contiguous fp16, bf16 or float32 CUDA tensor")
+    flags = REPACK_ZEROS_V2 if zeros_v2 else 0
+    if scales.dtype == torch.float32:
+        if dtype not in DTYPE:
+            raise GptqError(2, "float32 scales need dtype=torch.float16 or torch.bfloat16 (the layer's compute type)")
+        flags |= REPACK_SCALES_FP32
+    else:
+        dtype = scales.dtype if dtype is None else dtype
+        if dtype != scales.dtype:
+            raise GptqError(2, "16-bit scales must have the layer's dtype")
     if g_idx is not None and (g_idx.dtype != torch.int32 or not g_idx.is_contiguous() or not g_idx.is_cuda):
         raise GptqError(1, "g_idx must be a contiguous int32 CUDA tensor")
     out = C.c_void_p()
-    _check(lib().gptq_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
-                             DTYPE[scales.dtype], _stream(stream), C.byref(out)))
+    if flags:
+        _check(lib().gptq_repack_ex(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
+                                    DTYPE[dtype], flags, _stream(stream), C.byref(out)))
+    else:
+        _check(lib().gptq_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
+                                 DTYPE[dtype], _stream(stream), C.byref(out)))
     return Handle(out.value)
+
+
+def gptq_set_bias(h: Handle, bias: Optional[torch.Tensor], stream=None):
+    """Attach bias [N] (the handle's dtype or float32, on the device) to the handle; None detaches."""
+    if bias is None:
+        _check(lib().gptq_set_bias(h.ptr, None, 0, _stream(stream)))
+        return
+    info = gptq_get_info(h)
+    if bias.dim() != 1 or bias.numel() != info.N or not bias.is_contiguous() or not bias.is_cuda:
+        raise GptqError(3, f"bias must be a contiguous CUDA tensor of {info.N} elements")
+    handle_dt = torch.bfloat16 if info.dtype == 1 else torch.float16
+    if bias.dtype not in (handle_dt, torch.float32):
+        raise GptqError(2, f"bias must be {handle_dt} or float32")
+    _check(lib().gptq_set_bias(h.ptr, _ptr(bias), 1 if bias.dtype == torch.float32 else 0, _stream(stream)))
 
 
 def gptq_repack_awq(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor, group_size: int,
@@ -240,17 +276,22 @@ def gptq_copy_runtime(h: Handle) -> dict:
 class GptqLinear:
     """A GPTQ linear layer on the current CUDA device: repack once, then y = layer(x)."""
 
-    def __init__(self, qweight, qzeros, scales, g_idx, bits: int, group_size: int, stream=None, *, _handle=None):
+    def __init__(self, qweight, qzeros, scales, g_idx, bits: int, group_size: int, stream=None, *, bias=None,
+                 zeros_v2: bool = False, dtype: Optional[torch.dtype] = None, _handle=None):
         self.handle = _handle if _handle is not None else gptq_repack(qweight, qzeros, scales, g_idx, bits,
-                                                                        group_size, stream)
+                                                                        group_size, stream, zeros_v2=zeros_v2,
+                                                                        dtype=dtype)
         info = gptq_get_info(self.handle)
-        self.K, self.N, self.dtype = info.K, info.N, scales.dtype
+        self.K, self.N = info.K, info.N
+        self.dtype = torch.bfloat16 if info.dtype == 1 else torch.float16
+        if bias is not None:
+            gptq_set_bias(self.handle, bias, stream)
 
     @classmethod
-    def from_awq(cls, qweight, qzeros, scales, group_size: int, stream=None) -> "GptqLinear":
+    def from_awq(cls, qweight, qzeros, scales, group_size: int, stream=None, *, bias=None) -> "GptqLinear":
         """The same layer object built from an AutoAWQ GEMM checkpoint."""
-        return cls(None, None, scales, None, 4, group_size, _handle=gptq_repack_awq(qweight, qzeros, scales,
-                                                                                    group_size, stream))
+        return cls(None, None, scales, None, 4, group_size, bias=bias,
+                   _handle=gptq_repack_awq(qweight, qzeros, scales, group_size, stream))
 
     def __call__(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         if x.dtype != self.dtype or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
