@@ -591,3 +591,123 @@ int oracle_awq_to_gptq_fields(const int32_t* qweight, const int32_t* qzeros, int
     for (long n = 0; n < N; ++n) put_code(qzeros_gptq + g * (N / 8), 1, n, 4, awq_code(qzeros + g * (N / 8), n));
   return ORACLE_OK;
 }
+
+/*
+ * FP8 block-scaled checkpoints, [P4] ch. 39, section "FP8 checkpoints" (its quantize_blocks /
+ * dequantize_blocks description and the W8A16 kernel that widens the FP8 tiles and multiplies by
+ * the block's factor): weight float8_e4m3fn [N, K] (one byte per weight, row n holds input
+ * features 0..K-1), scale_inv float32 [ceil(N/128), ceil(K/128)], one factor per 128 x 128 block
+ * that multiplies the stored values:
+ *   W[n, k] = e4m3(weight[n, k]) * scale_inv[n / 128][k / 128]   (float32 product)
+ * E4M3 ("fn"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal
+ * (m * 2^-9); no infinities; exponent 15 with mantissa 7 is NaN; the largest value is 448.
+ */
+static float e4m3_value(uint8_t b) {
+  const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  float v;
+  if (e == 15 && m == 7) {
+    union { uint32_t u; float f; } q;
+    q.u = 0x7FC00000u;
+    return q.f;
+  }
+  if (e == 0) v = (float)m / 512.0f;                    /* m * 2^-9 */
+  else {
+    v = 1.0f + (float)m / 8.0f;
+    for (int i = 7; i < e; ++i) v *= 2.0f;              /* times 2^(e - 7), exact */
+    for (int i = e; i < 7; ++i) v *= 0.5f;
+  }
+  return sgn ? -v : v;
+}
+
+int oracle_e4m3_to_float(const uint8_t* in, long n, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = e4m3_value(in[i]);
+  return ORACLE_OK;
+}
+
+static int fp8_shape_ok(int K, int N) { return K > 0 && N > 0 && K % 32 == 0 && N % 32 == 0; }
+
+static void fp8_dequant_row(const uint8_t* weight, const float* scale_inv, int K, int N, long n, float* row) {
+  const long kb = (K + 127) / 128;
+  for (long k = 0; k < K; ++k) row[k] = e4m3_value(weight[n * K + k]) * scale_inv[(n / 128) * kb + k / 128];
+}
+
+/* Dense W float32 [N][K] of an FP8 block-scaled layer. */
+int oracle_fp8_dequant(const uint8_t* weight, const float* scale_inv, int K, int N, float* W) {
+  if (!fp8_shape_ok(K, N)) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(static)
+  for (long n = 0; n < N; ++n) fp8_dequant_row(weight, scale_inv, K, N, n, W + n * (long)K);
+  return ORACLE_OK;
+}
+
+/* y[r][c] = sum_k x[rows[r]][k] * W[cols[c]][k] in double, as oracle_linear. */
+int oracle_fp8_linear(const uint8_t* weight, const float* scale_inv, int dtype, int K, int N, const uint16_t* x,
+                      int M, const int32_t* rows, int nrows, const int32_t* cols, int ncols, double* y) {
+  if (!fp8_shape_ok(K, N)) return ORACLE_EINVAL;
+  for (int r = 0; r < nrows; ++r) if (rows[r] < 0 || rows[r] >= M) return ORACLE_EINVAL;
+  for (int c = 0; c < ncols; ++c) if (cols[c] < 0 || cols[c] >= N) return ORACLE_EINVAL;
+  float* xf = (float*)malloc(sizeof(float) * (size_t)nrows * K);
+  if (!xf) return ORACLE_EINVAL;
+  for (long r = 0; r < nrows; ++r)
+    for (long k = 0; k < K; ++k) xf[r * K + k] = half_bits_to_float(x[(long)rows[r] * K + k], dtype);
+  int fail = 0;
+#pragma omp parallel
+  {
+    float* row = (float*)malloc(sizeof(float) * (size_t)K);
+    if (!row) {
+#pragma omp atomic write
+      fail = 1;
+    } else {
+#pragma omp for schedule(static)
+      for (long c = 0; c < ncols; ++c) {
+        fp8_dequant_row(weight, scale_inv, K, N, cols[c], row);
+        for (long r = 0; r < nrows; ++r) {
+          double acc = 0.0;
+          const float* xr = xf + r * K;
+          for (long k = 0; k < K; ++k) acc += (double)xr[k] * (double)row[k];
+          y[r * ncols + c] = acc;
+        }
+      }
+      free(row);
+    }
+  }
+  free(xf);
+  return fail ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/*
+ * Runtime layout of an FP8 layer (this library's kernel-private format): the 8-bit layout of
+ * oracle_runtime_layout with sequential groups of 128 input features (one per scale block), except
+ * that the two bytes of a pair sit next to each other -- pair p of a lane word lives in its 16-bit
+ * half p % 2, the even k in the low byte -- so that one e4m3x2 conversion yields both halves of
+ * an MMA operand register.  wr, perm and cgid as in oracle_runtime_layout (sized by
+ * oracle_runtime_dims(NULL, K, N, 128)).
+ */
+int oracle_runtime_layout_fp8(const uint8_t* weight, int K, int N, uint8_t* wr, int32_t* perm, int32_t* cgid) {
+  int Kr, Np;
+  if (!fp8_shape_ok(K, N) || oracle_runtime_dims(NULL, K, N, 128, &Kr, &Np)) return ORACLE_EINVAL;
+  const int G = oracle_num_groups(K, 128);
+  long j = 0;
+  for (long c = 0; c < Kr / 32; ++c) cgid[c] = -1;
+  for (long i = 0; i < Kr; ++i) perm[i] = -1;
+  for (int g = 0; g < G; ++g) {
+    long start = j;
+    for (long k = 128L * g; k < K && k < 128L * (g + 1); ++k) perm[j++] = (int32_t)k;
+    j = start + (j - start + 31) / 32 * 32;
+    for (long c = start / 32; c < j / 32; ++c) cgid[c] = g;
+  }
+  for (long c = j / 32; c < Kr / 32; ++c) cgid[c] = cgid[j / 32 - 1];
+  memset(wr, 0, (size_t)Kr / 128 * 8 * Np * 16);
+  for (long jj = 0; jj < Kr; ++jj) {
+    long B = jj / 128, r = jj % 128, c = r / 32, t = (r % 32) / 8, e = r % 8;
+    long p = 4 * c + e / 2, h = e % 2;
+    long jw = p / 2, f = p % 2;
+    long q = t * 8 + jw, V = q / 4;
+    for (long n = 0; n < Np; ++n) {
+      uint32_t b = (perm[jj] >= 0 && n < N) ? weight[n * K + perm[jj]] : 0u;
+      long pos = n / 32 * 32 + (n % 32 + column_rotation(8, V)) % 32;
+      uint32_t* word = (uint32_t*)(wr + ((size_t)(B * 8 + V) * Np + pos) * 16 + 4 * (q % 4));
+      *word |= b << (16 * f + 8 * h);
+    }
+  }
+  return ORACLE_OK;
+}

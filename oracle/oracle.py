@@ -56,6 +56,10 @@ def lib():
                 "oracle_dequant_ex": [P, P, P, I, P, I, I, I, I, I, P],
                 "oracle_linear_ex": [P, P, P, I, P, I, I, I, I, I, P, I, P, I, P, I, P, I, P],
                 "oracle_round_fp32": [P, C.c_long, I, P],
+                "oracle_e4m3_to_float": [P, C.c_long, P],
+                "oracle_fp8_dequant": [P, P, I, I, P],
+                "oracle_fp8_linear": [P, P, I, I, I, P, I, P, I, P, I, P],
+                "oracle_runtime_layout_fp8": [P, I, I, P, P, P],
                 "oracle_check_rules": [I, I, I, I, I, I, I, I, P, I],
                 "oracle_runtime_dims": [P, I, I, I, P, P],
                 "oracle_runtime_layout": [P, P, P, P, I, I, I, I, P, P, P, P, P],
@@ -308,3 +312,54 @@ def awq_to_gptq_fields(qweight, qzeros, group_size: int) -> tuple[np.ndarray, np
     qzg = np.empty((G, N // 8), np.int32)
     _check(lib().oracle_awq_to_gptq_fields(_p(qw), _p(qz), K, N, group_size, _p(qwg), _p(qzg)), "awq_to_gptq_fields")
     return qwg, qzg
+
+
+# ---- FP8 block-scaled layers (float8_e4m3fn weight [N, K], float32 scale_inv per 128 x 128) ----
+
+def _fp8_bytes(weight) -> np.ndarray:
+    import torch
+    if isinstance(weight, torch.Tensor):
+        t = weight.detach().cpu().contiguous()
+        return t.view(torch.uint8).numpy() if t.dtype != torch.uint8 else t.numpy()
+    return np.ascontiguousarray(weight, np.uint8)
+
+
+def e4m3_to_float(codes) -> np.ndarray:
+    b = _fp8_bytes(codes)
+    out = np.empty(b.shape, np.float32)
+    _check(lib().oracle_e4m3_to_float(_p(b), b.size, _p(out)), "e4m3_to_float")
+    return out
+
+
+def fp8_dequant(weight, scale_inv) -> np.ndarray:
+    """Dense W float32 [N, K]."""
+    w, s = _fp8_bytes(weight), _np(scale_inv, np.float32)
+    N, K = w.shape
+    W = np.empty((N, K), np.float32)
+    _check(lib().oracle_fp8_dequant(_p(w), _p(s), K, N, _p(W)), "fp8_dequant")
+    return W
+
+
+def fp8_linear(weight, scale_inv, dtype: str, x, rows=None, cols=None) -> np.ndarray:
+    """y[rows][cols] = x[rows] . W[cols]^T in float64."""
+    w, s, xx = _fp8_bytes(weight), _np(scale_inv, np.float32), _np(x, np.uint16)
+    N, K = w.shape
+    M = xx.shape[0]
+    assert xx.shape[1] == K
+    r = np.arange(M, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+    c = np.arange(N, dtype=np.int32) if cols is None else np.ascontiguousarray(cols, np.int32)
+    y = np.empty((len(r), len(c)), np.float64)
+    _check(lib().oracle_fp8_linear(_p(w), _p(s), DT[dtype], K, N, _p(xx), M, _p(r), len(r), _p(c), len(c),
+                                   _p(y)), "fp8_linear")
+    return y
+
+
+def runtime_layout_fp8(weight) -> dict:
+    w = _fp8_bytes(weight)
+    N, K = w.shape
+    Kr, Np = runtime_dims(None, K, N, 128)
+    out = dict(Kr=Kr, Np=Np, G=num_groups(K, 128), wr=np.empty(Kr // 128 * 8 * Np * 16, np.uint8),
+               perm=np.empty(Kr, np.int32), cgid=np.empty(Kr // 32, np.int32))
+    _check(lib().oracle_runtime_layout_fp8(_p(w), K, N, _p(out["wr"]), _p(out["perm"]), _p(out["cgid"])),
+           "runtime_layout_fp8")
+    return out

@@ -125,6 +125,30 @@ def make_awq_checkpoint(K: int, N: int, group_size: int = 128, dtype: str = "fp1
     return AwqCheckpoint(K, N, group_size, dtype, qweight, qzeros, scales)
 
 
+@dataclasses.dataclass
+class Fp8Checkpoint:
+    """An FP8 block-scaled layer: float8_e4m3fn weight [N, K] (held as its bytes) and one float32
+    factor per 128 x 128 block."""
+    K: int
+    N: int
+    dtype: str                   # dtype of x and y
+    weight: torch.Tensor         # uint8 [N, K], e4m3 bit patterns
+    scale_inv: torch.Tensor      # float32 [ceil(N/128), ceil(K/128)]
+
+
+def make_fp8_checkpoint(K: int, N: int, dtype: str = "bf16", seed: int = 0, scale_lo: float = 1e-4,
+                        scale_hi: float = 1e-3) -> Fp8Checkpoint:
+    """Weight bytes uniform over the 254 e4m3 codes that are numbers (0x7F and 0xFF, the NaNs,
+    left out): every magnitude from the subnormals to 448 occurs, both signs.  Draw order:
+    weight bytes, scales."""
+    gen = torch.Generator().manual_seed(seed)
+    b = torch.randint(0, 254, (N, K), generator=gen, dtype=torch.int32)
+    b = b + (b >= 0x7F).to(torch.int32)                  # skip 0x7F; 0xFF is never reached
+    scale_inv = (torch.rand((-(-N // 128), -(-K // 128)), generator=gen, dtype=torch.float64)
+                 * (scale_hi - scale_lo) + scale_lo).float()
+    return Fp8Checkpoint(K, N, dtype, b.to(torch.uint8), scale_inv)
+
+
 def make_x(M: int, K: int, dtype: str, seed: int = 1) -> torch.Tensor:
     gen = torch.Generator().manual_seed(seed)
     return torch.randn((M, K), generator=gen, dtype=torch.float32).to(_DTYPES[dtype])
