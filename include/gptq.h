@@ -113,6 +113,25 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
  */
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
 
+/*
+ * Build a runtime handle from one FP8 block-scaled layer (inference.shantanugoel.com ch. 39,
+ * section "FP8 checkpoints": float8_e4m3fn weights with one float32 factor per 128 x 128 block,
+ * weight_scale_inv, which multiplies the stored values), for the W8A16 product:
+ *   W[n, k] = e4m3(weight[n, k]) * scale_inv[n / 128][k / 128],   y = x . W^T.
+ *   weight     device, float8_e4m3fn bytes [N, K] row-major (row n = output n).  Any alignment.
+ *              NaN codes (0x7F, 0xFF) are not checked and give NaN outputs.
+ *   scale_inv  device, float32 [ceil(N/128), ceil(K/128)] row-major.  4-byte aligned.
+ *   K, N       K % 32 == 0, N % 32 == 0 (as gptq_repack).   dtype: x and y.
+ * The weights are used exactly (every e4m3 number is an fp16 and a bf16 number); the products
+ * accumulate in fp32 per 128-wide block of K and are multiplied by the block's factor in fp32.
+ * The handle serves gptq_gemm, gptq_gemm_path, gptq_set_bias and the rest; gptq_get_info reports
+ * fp8 = 1, bits = 8, group_size = 128; gptq_copy_runtime gives zeros for s_r and z_r, which an
+ * FP8 handle does not keep.
+ * Errors: INVALID_ARG, UNSUPPORTED (dtype), SHAPE, ALIGNMENT, DEVICE, CUDA.
+ */
+gptq_status_t gptq_repack_fp8(const void* weight, const float* scale_inv, int K, int N, gptq_dtype_t dtype,
+                              void* stream, gptq_handle_t* out);
+
 /* Flags of gptq_repack_ex. */
 #define GPTQ_REPACK_ZEROS_V2    1u  /* qzeros fields hold the zero itself (the corrected gptq_v2
                                        layout named in ch. 39, "The format"), not zero - 1      */
@@ -207,6 +226,7 @@ typedef struct {
   int reserved_M;   /* largest M gptq_gemm accepts on every path without further reserve      */
   int zero_offset;  /* zero = stored zero field + zero_offset: 1 (GPTQ v1), 0 (gptq_v2, AWQ)     */
   int has_bias;     /* 1 while a bias is attached (gptq_set_bias)                              */
+  int fp8;          /* 1 for a handle built by gptq_repack_fp8                                 */
   size_t weight_bytes;     /* runtime codes: K_sorted/128 * bits * N_padded * 16              */
   size_t device_bytes;     /* everything the handle holds on the device                      */
 } gptq_info_t;

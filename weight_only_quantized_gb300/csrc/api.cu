@@ -30,8 +30,8 @@ gptq_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(GPTQ_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, bool awq, bool scales_fp32, cudaStream_t st);
+gptq_status_t build_runtime(Handle& h, const void* qweight, const int32_t* qzeros, const void* scales,
+                            const int32_t* g_idx, int fmt, bool scales_fp32, cudaStream_t st);
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -45,6 +45,7 @@ static void free_handle(Handle* h) {
   cudaFree(h->zst);
   cudaFree(h->xp);
   cudaFree(h->bias);
+  cudaFree(h->scale_inv);
   cudaFree(h->err);
   delete h;
 }
@@ -164,12 +165,14 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
 
 namespace gptq {
 // Argument checks shared by both checkpoint formats, then the handle and its runtime layout.
-static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, const void* scales,
                                  const int32_t* g_idx, int K, int N, int bits, int group_size, gptq_dtype_t dtype,
-                                 bool awq, unsigned flags, void* stream, gptq_handle_t* out) {
+                                 int fmt, unsigned flags, void* stream, gptq_handle_t* out) {
   if (!out) return fail(GPTQ_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  if (!qweight || !qzeros || !scales) return fail(GPTQ_ERR_INVALID_ARG, "qweight, qzeros and scales are required");
+  const bool fp8 = fmt == kFmtFp8;
+  if (!qweight || (!qzeros && !fp8) || !scales)
+    return fail(GPTQ_ERR_INVALID_ARG, fp8 ? "weight and scale_inv are required" : "qweight, qzeros and scales are required");
   if (bits != 2 && bits != 3 && bits != 4 && bits != 8)
     return fail(GPTQ_ERR_UNSUPPORTED, "GPTQ-001: bits must be 2, 3, 4 or 8, got " + std::to_string(bits));
   if (dtype != GPTQ_FP16 && dtype != GPTQ_BF16) return fail(GPTQ_ERR_UNSUPPORTED, "dtype must be GPTQ_FP16 or GPTQ_BF16");
@@ -183,8 +186,10 @@ static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, 
   if (flags & ~(unsigned)(GPTQ_REPACK_ZEROS_V2 | GPTQ_REPACK_SCALES_FP32))
     return fail(GPTQ_ERR_INVALID_ARG, "unknown repack flag bits");
   const bool sf32 = (flags & GPTQ_REPACK_SCALES_FP32) != 0;
-  if (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, sf32 ? 4 : 2) || (g_idx && !aligned(g_idx, 4)))
-    return fail(GPTQ_ERR_ALIGNMENT, "qweight, qzeros, g_idx need 4-byte and scales 2-byte (float32: 4-byte) alignment");
+  if (fp8 ? !aligned(scales, 4)
+          : (!aligned(qweight, 4) || !aligned(qzeros, 4) || !aligned(scales, sf32 ? 4 : 2) || (g_idx && !aligned(g_idx, 4))))
+    return fail(GPTQ_ERR_ALIGNMENT, fp8 ? "scale_inv needs 4-byte alignment"
+                                        : "qweight, qzeros, g_idx need 4-byte and scales 2-byte (float32: 4-byte) alignment");
   int dev = 0, sms = 0;
   gptq_status_t s = check_device(&dev, &sms);
   if (s != GPTQ_OK) return s;
@@ -195,11 +200,13 @@ static gptq_status_t repack_impl(const int32_t* qweight, const int32_t* qzeros, 
   h->K = K; h->N = N; h->bits = bits; h->group_size = group_size; h->G = G;
   h->Np = (N + 255) / 256 * 256;
   h->dtype = dtype;
-  h->zoff = (awq || (flags & GPTQ_REPACK_ZEROS_V2)) ? 0 : 1;
+  h->zoff = (fmt != kFmtGptq || (flags & GPTQ_REPACK_ZEROS_V2)) ? 0 : 1;
+  h->fp8 = fp8 ? 1 : 0;
+  h->kb = (K + 127) / 128;
   cudaError_t ce = cudaMalloc(&h->err, sizeof(int32_t));
   if (ce == cudaSuccess) ce = cudaMemsetAsync(h->err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaMalloc(error word)"); }
-  s = build_runtime(*h, qweight, qzeros, scales, g_idx, awq, sf32, static_cast<cudaStream_t>(stream));
+  s = build_runtime(*h, qweight, qzeros, scales, g_idx, fmt, sf32, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
   s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 32);
@@ -214,13 +221,13 @@ extern "C" {
 gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
                           int K, int N, int bits, int group_size, gptq_dtype_t dtype, void* stream,
                           gptq_handle_t* out) {
-  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, 0u, stream, out);
+  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, kFmtGptq, 0u, stream, out);
 }
 
 gptq_status_t gptq_repack_ex(const int32_t* qweight, const int32_t* qzeros, const void* scales, const int32_t* g_idx,
                              int K, int N, int bits, int group_size, gptq_dtype_t dtype, unsigned flags, void* stream,
                              gptq_handle_t* out) {
-  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, false, flags, stream, out);
+  return repack_impl(qweight, qzeros, scales, g_idx, K, N, bits, group_size, dtype, kFmtGptq, flags, stream, out);
 }
 
 gptq_status_t gptq_set_bias(gptq_handle_t hh, const void* bias, int bias_fp32, void* stream) {
@@ -251,7 +258,12 @@ gptq_status_t gptq_set_bias(gptq_handle_t hh, const void* bias, int bias_fp32, v
 
 gptq_status_t gptq_repack_awq(const int32_t* qweight, const int32_t* qzeros, const void* scales, int K, int N,
                               int group_size, gptq_dtype_t dtype, void* stream, gptq_handle_t* out) {
-  return repack_impl(qweight, qzeros, scales, nullptr, K, N, 4, group_size, dtype, true, 0u, stream, out);
+  return repack_impl(qweight, qzeros, scales, nullptr, K, N, 4, group_size, dtype, kFmtAwq, 0u, stream, out);
+}
+
+gptq_status_t gptq_repack_fp8(const void* weight, const float* scale_inv, int K, int N, gptq_dtype_t dtype,
+                              void* stream, gptq_handle_t* out) {
+  return repack_impl(weight, nullptr, scale_inv, nullptr, K, N, 8, 128, dtype, kFmtFp8, 0u, stream, out);
 }
 
 gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
@@ -323,9 +335,11 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->reserved_M = h.reserved_M;
   info->zero_offset = h.zoff;
   info->has_bias = h.has_bias;
+  info->fp8 = h.fp8;
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
-                       (size_t)h.G * h.Np * 6 + h.xp_bytes + (h.bias ? sizeof(float) * (size_t)h.Np : 0);
+                       (size_t)h.G * h.Np * (h.fp8 ? 3 : 6) + h.xp_bytes + (h.bias ? sizeof(float) * (size_t)h.Np : 0) +
+                       (h.scale_inv ? sizeof(float) * (size_t)((h.N + 127) / 128) * h.kb : 0);
   return GPTQ_OK;
 }
 
@@ -338,9 +352,12 @@ gptq_status_t gptq_copy_runtime(gptq_handle_t hh, void* wr, int32_t* perm, int32
     return cuda_fail(e, "copy perm");
   if (cgid && (e = cudaMemcpy(cgid, h.cgid, sizeof(int32_t) * (h.Kr / 32), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "copy cgid");
-  if (s_r && (e = cudaMemcpy(s_r, h.s_r, 2 * (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
+  // an FP8 handle keeps no per-column scales or zeros: those outputs read as zeros
+  if (s_r && !h.s_r) std::memset(s_r, 0, 2 * (size_t)h.G * h.Np);
+  if (z_r && !h.z_r) std::memset(z_r, 0, (size_t)h.G * h.Np);
+  if (s_r && h.s_r && (e = cudaMemcpy(s_r, h.s_r, 2 * (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "copy s_r");
-  if (z_r && (e = cudaMemcpy(z_r, h.z_r, (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
+  if (z_r && h.z_r && (e = cudaMemcpy(z_r, h.z_r, (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "copy z_r");
   return GPTQ_OK;
 }

@@ -93,6 +93,8 @@ struct LargeArgs {
   int M, N, Np, Kr, G;
   int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields; 0: gptq_v2, AWQ)
   const float* bias;   // [Np] float32 added to y, or nullptr
+  const float* scale_inv;   // FP8 layers: [ceil(N/128)][kb] block factors
+  int kb;
 };
 
 __device__ __forceinline__ uint32_t and_or_l(uint32_t a, uint32_t b, uint32_t c) {
@@ -222,9 +224,10 @@ __device__ __forceinline__ void reg_after_wait(uint32_t (&r)[16]) {
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                :: "memory");
 }
-template <typename T, int BITS, int BMX>
+template <typename T, int BITS, int BMX, bool FP8>
 __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, const __grid_constant__ CUtensorMap tmap_x) {
   static_assert(BMX == 64 || BMX == 128 || BMX == 256, "MMA N: a multiple of 16 up to 256; TMEM: a power of two");
+  static_assert(!FP8 || BITS == 8, "FP8 layers use the 8-bit layout");
   using S = LargeSmem<BITS, BMX>;
   constexpr int XB = X_BYTES<BMX>;
   constexpr int XS = gptq::XS<BITS, BMX>;
@@ -316,7 +319,11 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       ebits &= ebits - 1u;
       return 32 * ew + j;
     };
-    auto scale_of_end = [&](int e) { return e >= 0 ? scale_f<T>(__ldg(&a.s_r[(size_t)cg[e] * a.Np + n])) : 0.f; };
+    // (FP8: the CTA's 128 rows are one scale block; a block past N has no factor and stores nothing)
+    auto scale_of_end = [&](int e) {
+      if constexpr (FP8) return (e >= 0 && n0 < a.N) ? __ldg(&a.scale_inv[(size_t)(n0 / BN) * a.kb + cg[e]]) : 0.f;
+      else return e >= 0 ? scale_f<T>(__ldg(&a.s_r[(size_t)cg[e] * a.Np + n])) : 0.f;
+    };
     int ng = 0;                               // groups in K
     for (int w = 0; w < nwin; ++w) ng += __popc(gmask[w]);
     float sq[kSq];
@@ -425,13 +432,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         for (int blk = 0; blk < nblocks && ok; ++blk) {
           const int ps = blk % PS;
           if (blk >= PS && !mbar_wait(pk_empty(ps), ((blk / PS) - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(pk_full(ps), PKB);
+          mbar_arrive_expect_tx(pk_full(ps), FP8 ? (uint32_t)PK_BYTES<BITS> : (uint32_t)PKB);   // FP8: no zeros
           const uint8_t* src = a.wr + ((size_t)blk * BITS * a.Np + n0) * 16;
   #pragma unroll
           for (int v = 0; v < BITS; ++v)
             bulk_g2s(smem_u32(pk + ps * PKB + v * BN * 16), src + (size_t)v * a.Np * 16, BN * 16, pk_full(ps));
   #pragma unroll
-          for (int c = 0; c < 4; ++c)     // stored zeros of the block's chunks, 128 columns each
+          for (int c = 0; c < (FP8 ? 0 : 4); ++c)     // stored zeros of the block's chunks, 128 columns each
             bulk_g2s(smem_u32(pk + ps * PKB + PK_BYTES<BITS> + c * BN), a.z_r + (size_t)cg[4 * blk + c] * a.Np + n0,
                      BN, pk_full(ps));
           ++pk_issued;
@@ -503,8 +510,10 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         const int ps = blk % PS;
         if (!mbar_wait(pk_full(ps), (blk / PS) & 1)) { ok = false; break; }
         const uint8_t* stage = pk + ps * PKB;
+        if constexpr (!FP8) {
   #pragma unroll
-        for (int c = 0; c < 4; ++c) zq[c] = prep_zero_l<T, BITS>(stage[PK_BYTES<BITS> + c * BN + nrow], zoff);
+          for (int c = 0; c < 4; ++c) zq[c] = prep_zero_l<T, BITS>(stage[PK_BYTES<BITS> + c * BN + nrow], zoff);
+        }
         for (int h = 0; h < 2; ++h) {
           const int i = 2 * blk + h, ws = i % WS;
           if (i >= WS && !mbar_wait(w_empty(ws), ((i / WS) - 1) & 1)) { ok = false; break; }
@@ -518,10 +527,17 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
   #pragma unroll
             for (int t = 0; t < 4; ++t) {
               uint4 o;
-              o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[c]);
-              o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[c]);
-              o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[c]);
-              o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[c]);
+              if constexpr (FP8) {   // pairs 4c .. 4c + 3: words 2c, 2c + 1, halves 0 and 1
+                o.x = fp8_pair<T>(lw[t].w[2 * c], 0);
+                o.y = fp8_pair<T>(lw[t].w[2 * c], 1);
+                o.z = fp8_pair<T>(lw[t].w[2 * c + 1], 0);
+                o.w = fp8_pair<T>(lw[t].w[2 * c + 1], 1);
+              } else {
+                o.x = code_minus_zero<T, BITS>(lw[t], 4 * c + 0, zq[c]);
+                o.y = code_minus_zero<T, BITS>(lw[t], 4 * c + 1, zq[c]);
+                o.z = code_minus_zero<T, BITS>(lw[t], 4 * c + 2, zq[c]);
+                o.w = code_minus_zero<T, BITS>(lw[t], 4 * c + 3, zq[c]);
+              }
               const int j = 4 * cc + t;                         // 16-byte chunk (8 k) inside the 64-k row
               *reinterpret_cast<uint4*>(row + ((j ^ (nrow & 7)) << 4)) = o;
             }
@@ -562,11 +578,11 @@ template <int BITS, int BMX> size_t large_smem_bytes(int Kr) {
 // x rows per tile: the smallest of 64, 128, 256 that covers M (and 256 above it)
 inline int bmx_for(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
-template <typename T, int BITS, int BMX>
+template <typename T, int BITS, int BMX, bool FP8>
 cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
   const size_t smem = large_smem_bytes<BITS, BMX>(h.Kr);
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-  auto kern = k_gemm_large<T, BITS, BMX>;
+  auto kern = k_gemm_large<T, BITS, BMX, FP8>;
   // setmaxnreg redistributes the registers the block is launched with; a launch with fewer than
   // kRegsLaunch a thread could never satisfy the scalers' increase, so refuse it.
   static const int regs = [&] {
@@ -576,7 +592,8 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff, h.has_bias ? h.bias : nullptr};
+  LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff, h.has_bias ? h.bias : nullptr,
+                 h.scale_inv, h.kb};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, 1);     // consecutive CTAs share a weight tile
   cfg.blockDim = dim3(kThreadsL);
@@ -590,17 +607,18 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   return cudaLaunchKernelEx(&cfg, kern, args, map);
 }
 
-template <typename T, int BITS>
+template <typename T, int BITS, bool FP8 = false>
 cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
   switch (bmx_for(M)) {
-    case 64: return launch_tbm<T, BITS, 64>(h, map, y, M, st);
-    case 128: return launch_tbm<T, BITS, 128>(h, map, y, M, st);
-    default: return launch_tbm<T, BITS, 256>(h, map, y, M, st);
+    case 64: return launch_tbm<T, BITS, 64, FP8>(h, map, y, M, st);
+    case 128: return launch_tbm<T, BITS, 128, FP8>(h, map, y, M, st);
+    default: return launch_tbm<T, BITS, 256, FP8>(h, map, y, M, st);
   }
 }
 
 template <typename T>
 cudaError_t launch_t(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
+  if (h.fp8) return launch_tb<T, 8, true>(h, map, y, M, st);
   switch (h.bits) {
     case 2: return launch_tb<T, 2>(h, map, y, M, st);
     case 3: return launch_tb<T, 3>(h, map, y, M, st);

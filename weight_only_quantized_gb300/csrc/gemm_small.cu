@@ -273,8 +273,11 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
 }
 
-template <typename T, int BITS, int MT8, int CW, bool GATHER>
+template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8>
 __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
+  static_assert(!FP8 || (BITS == 8 && !GATHER), "FP8 layers: 8-bit layout, x staged without gather");
+  // the zero fold applies to integer codes; FP8 weights are their own values
+  constexpr bool kFZ = kFoldZero<T, BITS> && !FP8;
   constexpr int kCW = CW;
   constexpr int kThreadsS = threads_of<CW>();
   constexpr int SB = stage_bytes<BITS>();
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int i = 0; i < 2; ++i)
 #pragma unroll
       for (int mt = 0; mt < MT8; ++mt) {
-        if constexpr (kFoldZero<T, BITS>) {
+        if constexpr (kFZ) {
           acc[i][mt][0] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsv[mt].x, part[i][mt][0]), acc[i][mt][0]);
           acc[i][mt][1] = fmaf(sc[2 * i], fmaf(-zc[2 * i], xsv[mt].y, part[i][mt][1]), acc[i][mt][1]);
           acc[i][mt][2] = fmaf(sc[2 * i + 1], fmaf(-zc[2 * i + 1], xsv[mt].x, part[i][mt][2]), acc[i][mt][2]);
@@ -509,7 +512,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       // single-group blocks come from the all-ones MMAs and are kept in a table; later tiles read
       // them (x is the same for every tile) and skip those MMAs.
       auto run_blocks = [&](auto reuse_tag) {
-        constexpr bool kReuse = decltype(reuse_tag)::value && kFoldZero<T, BITS>;
+        constexpr bool kReuse = decltype(reuse_tag)::value && kFZ;
         for (int bs = (warp - kSPB * s_base) & (kCW - 1); bs < kSPB * nst && ok; bs += kCW) {
           const int js = bs / kSPB, u = bs % kSPB;
           const int s = s_base + js;
@@ -545,7 +548,12 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
               cur = gq;
 #pragma unroll
               for (int idx = 0; idx < 4; ++idx) {
-                if constexpr (kFoldZero<T, BITS>) {
+                if constexpr (FP8) {
+                  // the block's float32 factor, one for all 32 columns of the tile, in every zero slot
+                  (void)sw;
+                  sc[idx] = __uint_as_float(zw);
+                  continue;
+                } else if constexpr (kFZ) {
                   // magic + stored zero + zoff in fp32: one byte permute builds 2^23 + stored (exact),
                   // one add moves it (exact: integers below 2^24)
                   zc[idx] = __uint_as_float(__byte_perm(zw, 0x4B000000u, 0x7440u + idx)) - zsub;
@@ -553,8 +561,10 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
                   zq[idx] = prep_zero<T, BITS>((zw >> (8 * idx)) & 0xFFu, (uint32_t)a.zoff);
                 }
               }
-              sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
-              sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+              if constexpr (!FP8) {
+                sc[0] = to_float<T>(sw.x & 0xFFFFu); sc[1] = to_float<T>(sw.x >> 16);
+                sc[2] = to_float<T>(sw.y & 0xFFFFu); sc[3] = to_float<T>(sw.y >> 16);
+              }
             };
             auto load_group = [&](const int gq) {
               const uint8_t* zrow = zs + (gq - gf) * kZsRow;
@@ -573,7 +583,12 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                   uint32_t af[4];
-                  if constexpr (kFoldZero<T, BITS>) {
+                  if constexpr (FP8) {
+                    af[0] = fp8_pair<T>(lw[2 * i].w[p0 / 2], p0 % 2);
+                    af[1] = fp8_pair<T>(lw[2 * i + 1].w[p0 / 2], p0 % 2);
+                    af[2] = fp8_pair<T>(lw[2 * i].w[(p0 + 1) / 2], (p0 + 1) % 2);
+                    af[3] = fp8_pair<T>(lw[2 * i + 1].w[(p0 + 1) / 2], (p0 + 1) % 2);
+                  } else if constexpr (kFZ) {
                     af[0] = operand_raw<T, BITS>(lw[2 * i], p0);
                     af[1] = operand_raw<T, BITS>(lw[2 * i + 1], p0);
                     af[2] = operand_raw<T, BITS>(lw[2 * i], p0 + 1);
@@ -590,7 +605,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
                     else mma16816<T>(part[i][mt], af, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
                   }
                 }
-                if constexpr (kFoldZero<T, BITS> && kOnes) {
+                if constexpr (kFZ && kOnes) {
                   const uint32_t ones[4] = {kOnes2<T>, kOnes2<T>, kOnes2<T>, kOnes2<T>};
 #pragma unroll
                   for (int mt = 0; mt < MT8; ++mt) {
@@ -620,7 +635,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt) {
                   xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
-                  if (kFoldZero<T, BITS> && g == 0)
+                  if (kFZ && g == 0)
                     *reinterpret_cast<float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t) = xsv[mt];
                 }
               }
@@ -784,11 +799,11 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
 // weight ring keeps at least eight stages; otherwise a pre-pass gathers x into the workspace.
 bool make_plan(const Handle& h, int M, SmallPlan& p) {
   const int mt8 = M <= 8 ? 1 : M <= 16 ? 2 : 4;
-  if (!h.identity && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
+  if (!h.identity && !h.fp8 && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
   return plan_layout(h, M, h.bits, mt8, false, p);
 }
 
-template <typename T, int BITS, int MT8>
+template <typename T, int BITS, int MT8, bool FP8>
 cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
   SmallPlan p{};
   {
@@ -797,11 +812,13 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
     auto it = h.plans.find(key);
     if (it == h.plans.end()) {
       if (!make_plan(h, M, p)) return cudaErrorInvalidConfiguration;
-      cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if constexpr (MT8 == 1) {
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if constexpr (!FP8) {
+          if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+          if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        }
       }
       if (e != cudaSuccess) return e;
       std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
@@ -842,24 +859,27 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if constexpr (MT8 == 1) {
-    if (p.gather)
-      return p.cw == 16 ? cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true>, args, h.wr_map)
-                        : cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, true>, args, h.wr_map);
-    if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false>, args, h.wr_map);
+    if constexpr (!FP8) {
+      if (p.gather)
+        return p.cw == 16 ? cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true, false>, args, h.wr_map)
+                          : cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, true, false>, args, h.wr_map);
+    }
+    if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false, FP8>, args, h.wr_map);
   }
-  return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false>, args, h.wr_map);
+  return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8>, args, h.wr_map);
 }
 
-template <typename T, int BITS>
+template <typename T, int BITS, bool FP8 = false>
 cudaError_t launch_bits(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  if (M <= 8) return launch_t<T, BITS, 1>(h, x, y, M, st);
-  if (M <= 16) return launch_t<T, BITS, 2>(h, x, y, M, st);
-  if (M <= 32) return launch_t<T, BITS, 4>(h, x, y, M, st);
+  if (M <= 8) return launch_t<T, BITS, 1, FP8>(h, x, y, M, st);
+  if (M <= 16) return launch_t<T, BITS, 2, FP8>(h, x, y, M, st);
+  if (M <= 32) return launch_t<T, BITS, 4, FP8>(h, x, y, M, st);
   return cudaErrorInvalidValue;
 }
 
 template <typename T>
 cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
+  if (h.fp8) return launch_bits<T, 8, true>(h, x, y, M, st);
   switch (h.bits) {
     case 2: return launch_bits<T, 2>(h, x, y, M, st);
     case 3: return launch_bits<T, 3>(h, x, y, M, st);

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <type_traits>
 #include <vector>
 
 #include "../../include/gptq.h"
@@ -33,6 +34,10 @@ struct Handle {
   uint8_t* z_r = nullptr;    // [G][Np] stored zero field (GPTQ: zero - 1; AWQ: the zero itself)
   int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ v1 fields, 0 for gptq_v2 and AWQ
   float* bias = nullptr;     // [Np] float32 bias added to y (pad columns 0), allocated by gptq_set_bias
+  // FP8 block-scaled layers (codes are e4m3 bytes; no zeros; s_r and z_r are not allocated)
+  int fp8 = 0;
+  float* scale_inv = nullptr;   // [ceil(N/128)][kb] float32, one factor per 128 x 128 block
+  int kb = 0;                   // ceil(K/128)
   int has_bias = 0;          // 1: the GEMM kernels add bias
   uint8_t* zst = nullptr;    // [Np/32][G][96]: per 32-column tile and group, 32 stored zeros then
                              // 32 scales, column c at position (c % 8) * 4 + c / 8 (small-M path)
@@ -64,6 +69,24 @@ __host__ __device__ __forceinline__ int code_col_pos(int bits, int v, int n) {
   return (n & ~31) | (((n & 31) + code_col_rot(bits, v)) & 31);
 }
 
+// FP8 layers: the runtime layout keeps a pair's two e4m3 bytes side by side in one 16-bit half of a
+// lane word (the even k in the low byte).  One conversion gives the exact fp16 pair; for bf16 the
+// fp16 bits move into bf16 position as the value times 2^-112 (every e4m3 number is a normal fp16,
+// 2^-9 .. 448, whose low seven mantissa bits are zero, so the shifted fields are exact and never
+// subnormal), the sign is put back, and one exact multiply by 2^112 restores the value.
+template <typename T>
+__device__ __forceinline__ uint32_t fp8_pair(uint32_t word, int half) {
+  uint32_t d;
+  if (half == 0) asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.rn.f16x2.e4m3x2 %0, lo; }" : "=r"(d) : "r"(word));
+  else asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.rn.f16x2.e4m3x2 %0, hi; }" : "=r"(d) : "r"(word));
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    uint32_t t;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(d >> 3), "r"(0x0FFF0FFFu), "r"(d & 0x80008000u));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x77807780u));   // 2^112 in both halves
+  }
+  return d;
+}
+
 // cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -75,6 +98,9 @@ gptq_status_t fail(gptq_status_t s, const std::string& msg);
 gptq_status_t cuda_fail(cudaError_t e, const char* what);
 
 // ---- kernels launched from the host code (defined in the .cu files) ----
+
+// Checkpoint formats the repack reads.
+enum Format { kFmtGptq = 0, kFmtAwq = 1, kFmtFp8 = 2 };
 
 // bias[n] -> float32 [Np] (kind 0 fp16, 1 bf16, 2 float32; pad columns 0), enqueued on st.
 cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst, cudaStream_t st);

@@ -169,10 +169,14 @@ __global__ void k_pads(int G, int Ks, int Kr, int last_g, const int32_t* __restr
   }
 }
 
-// One thread per (block B, vector V, column n): assembles that 16-byte vector.  awq: qweight is an
-// AutoAWQ [K, N/8] tensor (4-bit) instead of the GPTQ [K*bits/32, N] one.
-__global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t* __restrict__ perm,
-                             int N, int Np, int bits, int nBV, int awq, uint8_t* __restrict__ wr) {
+// One thread per (block B, vector V, column n): assembles that 16-byte vector.  fmt: kFmtGptq reads
+// qweight as the GPTQ [K*bits/32, N] tensor, kFmtAwq as an AutoAWQ [K, N/8] one (4-bit), kFmtFp8 as
+// e4m3 bytes [N, K] (8-bit), whose pairs keep their two bytes side by side in one 16-bit half (pair
+// p in half p % 2, the even k in the low byte) so that one e4m3x2 conversion makes an operand.
+__global__ void k_pack_codes(const void* __restrict__ qweight_v, const int32_t* __restrict__ perm, int K,
+                             int N, int Np, int bits, int nBV, int fmt, uint8_t* __restrict__ wr) {
+  const int32_t* qweight = static_cast<const int32_t*>(qweight_v);
+  const uint8_t* w8 = static_cast<const uint8_t*>(qweight_v);
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= Np) return;
   for (int by = blockIdx.y; by < nBV; by += gridDim.y) {
@@ -192,9 +196,11 @@ __global__ void k_pack_codes(const int32_t* __restrict__ qweight, const int32_t*
         const int jj = 128 * B + 32 * c + 8 * t + e;
         const int k = __ldg(&perm[jj]);
         uint32_t code = 0u;
-        if (k >= 0 && n < N) code = awq ? awq_code(qweight + (long)k * (N / 8), n) : column_code(qweight + n, N, k, bits);
+        if (k >= 0 && n < N)
+          code = fmt == kFmtFp8 ? (uint32_t)__ldg(&w8[(long)n * K + k])
+               : fmt == kFmtAwq ? awq_code(qweight + (long)k * (N / 8), n) : column_code(qweight + n, N, k, bits);
         uint32_t val = bits == 3 ? (plane == 0 ? (code & 3u) : (code >> 2)) : code;
-        word |= val << (16 * h + bp * f);
+        word |= val << (fmt == kFmtFp8 ? 16 * f + 8 * h : 16 * h + bp * f);
       }
     out[w] = word;
   }
@@ -246,6 +252,20 @@ __global__ void k_pack_zst(const uint16_t* __restrict__ s_r, const uint8_t* __re
   }
 }
 
+// FP8 layers: every (32-column tile T, group g) row of zst carries the block's float32 factor
+// scale_inv[32 T / 128][g] in each of its eight 4-byte zero slots (the slot lane group g8 of the
+// small-M kernel reads), and zeros elsewhere; tiles past N get 0.
+__global__ void k_pack_zst_fp8(const float* __restrict__ scale_inv, int kb, int N, int Np, int G,
+                               uint8_t* __restrict__ zst) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;      // one thread per (T, g) row
+  if (i >= (Np / 32) * G) return;
+  const int T = i / G, g = i % G;
+  const float s = 32 * T < N ? __ldg(&scale_inv[(long)(32 * T / 128) * kb + g]) : 0.0f;
+  uint32_t* row = reinterpret_cast<uint32_t*>(zst + (size_t)i * 96);
+  for (int w = 0; w < 8; ++w) row[w] = __float_as_uint(s);
+  for (int w = 8; w < 24; ++w) row[w] = 0u;
+}
+
 // bias[n] as float32 (0 for the pad columns n >= N): kind 0 fp16 bits, 1 bf16 bits, 2 float32.
 __global__ void k_bias_f32(const void* __restrict__ src, int kind, int N, int Np, float* __restrict__ dst) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
@@ -268,8 +288,8 @@ cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst
   return cudaGetLastError();
 }
 
-gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qzeros, const void* scales,
-                            const int32_t* g_idx, bool awq, bool scales_fp32, cudaStream_t st) {
+gptq_status_t build_runtime(Handle& h, const void* qweight, const int32_t* qzeros, const void* scales,
+                            const int32_t* g_idx, int fmt, bool scales_fp32, cudaStream_t st) {
   const int K = h.K, N = h.N, G = h.G;
   int32_t* tmp = nullptr;   // cnt[G] | off[G] | cursor[G] | meta[M_N]
   cudaError_t e = cudaMalloc(&tmp, sizeof(int32_t) * ((size_t)3 * G + M_N));
@@ -298,10 +318,13 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   const int Ks = meta_h[M_KS], last_g = meta_h[M_LAST_G];
 
   size_t wr_b = h.wr_bytes();
+  const bool fp8 = fmt == kFmtFp8;
+  const size_t nsc = fp8 ? (size_t)((N + 127) / 128) * h.kb : 0;
   if ((e = cudaMalloc(&h.wr, wr_b)) != cudaSuccess || (e = cudaMalloc(&h.perm, sizeof(int32_t) * h.Kr)) != cudaSuccess ||
       (e = cudaMalloc(&h.cgid, sizeof(int32_t) * (h.Kr / 32))) != cudaSuccess ||
-      (e = cudaMalloc(&h.s_r, sizeof(uint16_t) * (size_t)G * h.Np)) != cudaSuccess ||
-      (e = cudaMalloc(&h.z_r, (size_t)G * h.Np)) != cudaSuccess ||
+      (!fp8 && (e = cudaMalloc(&h.s_r, sizeof(uint16_t) * (size_t)G * h.Np)) != cudaSuccess) ||
+      (!fp8 && (e = cudaMalloc(&h.z_r, (size_t)G * h.Np)) != cudaSuccess) ||
+      (fp8 && (e = cudaMalloc(&h.scale_inv, sizeof(float) * nsc)) != cudaSuccess) ||
       (e = cudaMalloc(&h.zst, (size_t)G * h.Np * 3)) != cudaSuccess) {
     cleanup();
     return cuda_fail(e, "cudaMalloc(runtime layout)");
@@ -326,12 +349,21 @@ gptq_status_t build_runtime(Handle& h, const int32_t* qweight, const int32_t* qz
   k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, h.Kr, last_g, cnt, off, h.perm, h.cgid);
   const int nBV = (h.Kr / 128) * h.bits;
   dim3 gc(h.Np / 256, nBV < 65535 ? nBV : 65535);
-  k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, N, h.Np, h.bits, nBV, awq ? 1 : 0, h.wr);
-  dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
-  k_pack_sz<<<gs, 256, 0, st>>>(qzeros, scales, N, h.Np, h.bits, G, awq ? 1 : 0, scales_fp32 ? 1 : 0,
-                                h.dtype == GPTQ_BF16 ? 1 : 0, h.s_r, h.z_r);
-  dim3 gz(h.Np / 32 / 8, G < 65535 ? G : 65535);
-  k_pack_zst<<<gz, 256, 0, st>>>(h.s_r, h.z_r, h.Np, G, h.zst);
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, h.perm, K, N, h.Np, h.bits, nBV, fmt, h.wr);
+  if (fp8) {
+    if ((e = cudaMemcpyAsync(h.scale_inv, scales, sizeof(float) * nsc, cudaMemcpyDeviceToDevice, st)) != cudaSuccess) {
+      cleanup();
+      return cuda_fail(e, "copy scale_inv");
+    }
+    const int rows = (h.Np / 32) * G;
+    k_pack_zst_fp8<<<(rows + 255) / 256, 256, 0, st>>>(static_cast<const float*>(scales), h.kb, N, h.Np, G, h.zst);
+  } else {
+    dim3 gs(h.Np / 256, G < 65535 ? G : 65535);
+    k_pack_sz<<<gs, 256, 0, st>>>(qzeros, scales, N, h.Np, h.bits, G, fmt == kFmtAwq ? 1 : 0, scales_fp32 ? 1 : 0,
+                                  h.dtype == GPTQ_BF16 ? 1 : 0, h.s_r, h.z_r);
+    dim3 gz(h.Np / 32 / 8, G < 65535 ? G : 65535);
+    k_pack_zst<<<gz, 256, 0, st>>>(h.s_r, h.z_r, h.Np, G, h.zst);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) { cleanup(); return cuda_fail(e, "repack launch"); }
   h.cgid_host.resize(h.Kr / 32);
   if ((e = cudaMemcpyAsync(h.cgid_host.data(), h.cgid, sizeof(int32_t) * (h.Kr / 32), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
@@ -437,7 +469,7 @@ extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32
   k_pads<<<(G + 127) / 128, 128, 0, st>>>(G, Ks, Kr, last_g, cnt, off, perm, cgid);
   const int nBV = (Kr / 128) * bits;
   dim3 gc(Np / 256, nBV < 65535 ? nBV : 65535);
-  k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, N, Np, bits, nBV, 0, static_cast<uint8_t*>(wr));
+  k_pack_codes<<<gc, 256, 0, st>>>(qweight, perm, K, N, Np, bits, nBV, kFmtGptq, static_cast<uint8_t*>(wr));
   dim3 gs(Np / 256, G < 65535 ? G : 65535);
   k_pack_sz<<<gs, 256, 0, st>>>(qzeros, scales, N, Np, bits, G, 0, 0, 0, static_cast<uint16_t*>(s_r), z_r);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "repack launch");

@@ -33,7 +33,8 @@ _P, _I, _L = C.c_void_p, C.c_int, C.c_int64
 class GptqInfo(C.Structure):
     _fields_ = [("K", C.c_int), ("N", C.c_int), ("bits", C.c_int), ("group_size", C.c_int), ("G", C.c_int),
                 ("K_sorted", C.c_int), ("N_padded", C.c_int), ("identity", C.c_int), ("dtype", C.c_int),
-                ("reserved_M", C.c_int), ("zero_offset", C.c_int), ("has_bias", C.c_int), ("weight_bytes", C.c_size_t),
+                ("reserved_M", C.c_int), ("zero_offset", C.c_int), ("has_bias", C.c_int), ("fp8", C.c_int),
+                ("weight_bytes", C.c_size_t),
                 ("device_bytes", C.c_size_t)]
 
 
@@ -43,6 +44,7 @@ SIGNATURES = {
     "gptq_repack_awq": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "gptq_repack_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, C.c_uint, _P, _P]),
     "gptq_set_bias": (_I, [_P, _P, _I, _P]),
+    "gptq_repack_fp8": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "gptq_reserve": (_I, [_P, _I]),
     "gptq_gemm": (_I, [_P, _P, _P, _I, _P]),
     "gptq_gemm_path": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -207,6 +209,23 @@ def gptq_repack_awq(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.T
     return Handle(out.value)
 
 
+def gptq_repack_fp8(weight: torch.Tensor, scale_inv: torch.Tensor, dtype: torch.dtype, stream=None) -> Handle:
+    """FP8 block-scaled layer (weight float8_e4m3fn or its uint8 bytes [N, K], scale_inv float32
+    [ceil(N/128), ceil(K/128)], on the current CUDA device) -> runtime handle computing in dtype."""
+    if weight.dim() != 2 or weight.element_size() != 1 or not weight.is_contiguous() or not weight.is_cuda:
+        raise GptqError(1, "weight must be a contiguous 2-d float8_e4m3fn (or uint8) CUDA tensor")
+    if scale_inv.dtype != torch.float32 or not scale_inv.is_contiguous() or not scale_inv.is_cuda:
+        raise GptqError(1, "scale_inv must be a contiguous float32 CUDA tensor")
+    if dtype not in DTYPE:
+        raise GptqError(2, "dtype must be torch.float16 or torch.bfloat16")
+    N, K = weight.shape
+    if tuple(scale_inv.shape) != (-(-N // 128), -(-K // 128)):
+        raise GptqError(3, f"scale_inv must be [{-(-N // 128)}, {-(-K // 128)}] for a [{N}, {K}] weight")
+    out = C.c_void_p()
+    _check(lib().gptq_repack_fp8(_ptr(weight), _ptr(scale_inv), K, N, DTYPE[dtype], _stream(stream), C.byref(out)))
+    return Handle(out.value)
+
+
 def gptq_reserve(h: Handle, max_M: int):
     _check(lib().gptq_reserve(h.ptr, max_M))
 
@@ -286,6 +305,18 @@ class GptqLinear:
         self.dtype = torch.bfloat16 if info.dtype == 1 else torch.float16
         if bias is not None:
             gptq_set_bias(self.handle, bias, stream)
+
+    @classmethod
+    def from_fp8(cls, weight, scale_inv, dtype: torch.dtype, stream=None, *, bias=None) -> "GptqLinear":
+        """The same layer object built from an FP8 block-scaled checkpoint (W8A16)."""
+        h = gptq_repack_fp8(weight, scale_inv, dtype, stream)
+        obj = cls.__new__(cls)
+        obj.handle = h
+        info = gptq_get_info(h)
+        obj.K, obj.N, obj.dtype = info.K, info.N, dtype
+        if bias is not None:
+            gptq_set_bias(h, bias, stream)
+        return obj
 
     @classmethod
     def from_awq(cls, qweight, qzeros, scales, group_size: int, stream=None, *, bias=None) -> "GptqLinear":
