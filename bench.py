@@ -391,6 +391,7 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
     s4, m4 = synth.workload("prefill-8192x28672-b4g128")
     one("prefill-8192x28672-b4g128", s4, [4096] if args.quick_prefill else m4, 1)
     out["awq-4096x14336-b4g128-fp16"] = awq_layer(hbm, tf_burst)
+    out["fp8-4096x14336-block128-bf16"] = fp8_layer(hbm, tf_burst)
     if not args.no_sweep:
         out["format-sweep-4096x4096"] = format_sweep(hbm, tf_burst)
     out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "kind": peak_kind}
@@ -423,6 +424,38 @@ def awq_layer(hbm, tf_burst):
     for h in hs:
         h.close()
     del hs, dev
+    torch.cuda.empty_cache()
+    return r
+
+
+def fp8_layer(hbm, tf_burst):
+    """An FP8 block-scaled layer of the decode layer's shape (K = 4096, N = 14336, e4m3 weights, one
+    float32 factor per 128 x 128 block, bf16 x and y) through gptq_repack_fp8 at M = 1, 16 and 512;
+    16 handles rotated (940 MB of weights) so every call streams from HBM.  Bytes per call: the
+    weight bytes, the factors, x and y."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    K, N = 4096, 14336
+    ck = synth.make_fp8_checkpoint(K, N, "bf16", seed=6)
+    w, s = ck.weight.cuda(), ck.scale_inv.cuda()
+    hs = [gptq.gptq_repack_fp8(w, s, torch.bfloat16) for _ in range(LAYERS)]
+    del w, s
+    torch.cuda.synchronize()
+    r = {"layers_rotated": LAYERS}
+    for M in (1, 16, 512):
+        xs = [synth.make_x(M, K, "bf16", seed=M + i).cuda() for i in range(4)]
+        ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+        t = time_calls(hs, xs, ys, M, 200 if M <= 64 else 50, 3, graph=True)
+        B = N * K + 4 * (-(-N // 128)) * (-(-K // 128)) + 2 * M * K + 2 * M * N
+        F = 2.0 * M * N * K
+        roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
+        r[f"M={M}"] = {"us": round(t * 1e6, 2), "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),
+                       "roofline_frac": round(roof / t, 4),
+                       "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+        del xs, ys
+    for h in hs:
+        h.close()
+    del hs
     torch.cuda.empty_cache()
     return r
 
