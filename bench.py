@@ -309,7 +309,7 @@ def run_native(args, ws, rank, local):
         torch.cuda.synchronize()
         e2e_t = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3 / args.steps)
         barrier(ws)
-        extra = {} if (args.no_extra or rank != 0) else extra_workloads(args, hbm, tf_burst, peak_kind)
+        extra = {} if (args.no_extra or rank != 0) else extra_workloads(args, hbm, tf_burst, peak_kind, tf_sus)
     clocks = clk.summary()
     bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(clocks["reasons"])
     if bad and not args._remeasured:
@@ -345,6 +345,12 @@ def run_native(args, ws, rank, local):
         gbs, calls, secs, cores, sample = oracle_sample_rate(spec, M, args.cpu_seconds, 2048)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
+        # the same oracle on one host core (a separate figure; the line's value is the all-core one)
+        import oracle
+        oracle.set_num_threads(1)
+        g1, _, _, _, s1 = oracle_sample_rate(spec, M, args.cpu_seconds / 2, 256)
+        oracle.set_num_threads(cores)
+        line["cpu_baseline"]["one_core"] = {"value": round(g1, 4), "unit": "GB/s", "sample": s1}
     if extra:
         line["detail"] = extra
     if rank == 0:
@@ -354,7 +360,31 @@ def run_native(args, ws, rank, local):
     return 0
 
 
-def extra_workloads(args, hbm, tf_burst, peak_kind):
+def repack_times():
+    """Load-time repack (checkpoint -> runtime layout) per layer, timed apart from the GEMM: host wall
+    clock around each repack call (it ends with a stream synchronize), median of three."""
+    import torch
+    from weight_only_quantized_gb300 import gptq, synth
+    out = {}
+    for name in ("llama3-8b-decode-4096x14336-b4g128-sym", "llama3-70b-gate-8192x28672-b4g128-descact"):
+        spec, _ = synth.workload(name)
+        ck = synth.make_checkpoint(spec, seed=3)
+        d = [t.cuda() if t is not None else None for t in (ck.qweight, ck.qzeros, ck.scales, ck.g_idx)]
+        ts = []
+        for _ in range(4):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            h = gptq.gptq_repack(d[0], d[1], d[2], d[3], spec.bits, spec.group_size)
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+            h.close()
+        ts = sorted(ts[1:])
+        out[name] = {"ms": round(ts[1] * 1e3, 3), "weight_MB": round(spec.K * spec.N * spec.bits / 8 / 1e6, 1)}
+        del d
+    return out
+
+
+def extra_workloads(args, hbm, tf_burst, peak_kind, tf_sus):
     """Rank 0: the other M values of the decode layer, the 70B gate layer, and prefill."""
     import torch
     from weight_only_quantized_gb300 import gptq, synth
@@ -378,6 +408,9 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
             res[f"M={M}"] = {"us": round(launch * 1e6, 2), "GB/s": round(B / launch / 1e9, 1),
                              "TFLOP/s": round(F / launch / 1e12, 2), "roofline_frac": round(roof / launch, 4),
                              "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+            if res[f"M={M}"]["bound"] == "tensor":
+                # against the sustained (power-capped) bf16 rate as well as the burst one
+                res[f"M={M}"]["roofline_frac_sustained"] = round(max(B / (hbm * 1e9), F / (tf_sus * 1e12)) / launch, 4)
             del xs, ys
         for h in hs:
             h.close()
@@ -394,7 +427,8 @@ def extra_workloads(args, hbm, tf_burst, peak_kind):
     out["fp8-4096x14336-block128-bf16"] = fp8_layer(hbm, tf_burst)
     if not args.no_sweep:
         out["format-sweep-4096x4096"] = format_sweep(hbm, tf_burst)
-    out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "kind": peak_kind}
+    out["repack"] = repack_times()
+    out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf_burst, "bf16_tflops_sustained": tf_sus, "kind": peak_kind}
     return out
 
 

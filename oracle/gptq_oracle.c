@@ -341,6 +341,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Thread count for the parallel loops that follow (a measurement setting; no arithmetic changes). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /*
  * Reject rules of [P5] "Reject the file when", as far as shapes and values decide them.
  * Returns 0 when accepted, else the rule number (1..4) that rejects:

@@ -64,6 +64,7 @@ def lib():
                 "oracle_runtime_dims": [P, I, I, I, P, P],
                 "oracle_runtime_layout": [P, P, P, P, I, I, I, I, P, P, P, P, P],
                 "oracle_num_threads": [],
+                "oracle_set_num_threads": [I],
                 "oracle_awq_unpack": [P, I, I, P],
                 "oracle_awq_pack": [P, I, I, P],
                 "oracle_awq_dequant": [P, P, P, I, I, I, I, P],
@@ -74,6 +75,7 @@ def lib():
                 f = getattr(L, name)
                 f.argtypes = args
                 f.restype = I
+            L.oracle_set_num_threads.restype = None
             L.oracle_half_to_float.argtypes = [C.c_uint16, I]
             L.oracle_half_to_float.restype = C.c_float
             _lib = L
@@ -254,6 +256,11 @@ def runtime_layout(qweight, qzeros, scales, g_idx, bits: int, group_size: int) -
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Thread count of the following oracle calls (timing only; results do not depend on it)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def half_to_float(bits_u16: int, dtype: str) -> float:
