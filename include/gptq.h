@@ -108,8 +108,12 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
  * Make gptq_gemm calls with M <= max_M possible without any allocation inside gptq_gemm.
  * Only a handle whose g_idx order is not the identity (act-order, or groups whose sizes are
  * not multiples of 32) needs workspace above M = 32: max_M * K_sorted activation elements for
- * the permuted copy of x that the kernels read.  Allocates (cudaMalloc) outside any
- * stream capture; never shrinks.  Errors: INVALID_ARG, CUDA.
+ * the permuted copy of x that the kernels read.  It also sizes the large-M kernel's K-split
+ * workspace for every M <= max_M whose grid would leave SMs idle (fewer tiles than SMs, or a
+ * mostly empty last wave): fp32 partials of at most 64 MB and one int32 counter per output tile.
+ * Calls with an M this has not covered run without a K split (same results, slower at those M).
+ * Allocates (cudaMalloc) outside any stream capture; never shrinks; the handle's device must be
+ * current.  Errors: INVALID_ARG, CUDA.
  */
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
 
@@ -211,6 +215,10 @@ gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gpt
 /* Number of kernels one gptq_gemm_path call at this M launches (0 for M == 0), or -1 on a bad
  * argument.  Host only. */
 int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
+
+/* Number of K ranges the large-M kernel splits a call at this M into (1 = none; more only where
+ * gptq_reserve covered M), or -1 on a bad argument.  Host only. */
+int gptq_gemm_k_splits(gptq_handle_t h, int M);
 
 /* Free the handle and everything it owns.  Waits for the device to finish using it
  * (cudaDeviceSynchronize on the handle's device).  NULL is accepted. */

@@ -2,6 +2,9 @@
 // checkpoint", section "Reject the file when"), handle lifecycle, and the per-call M dispatch.
 #include "internal.cuh"
 
+#include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <string>
@@ -46,6 +49,8 @@ static void free_handle(Handle* h) {
   cudaFree(h->xp);
   cudaFree(h->bias);
   cudaFree(h->scale_inv);
+  cudaFree(h->ws);
+  cudaFree(h->ws_cnt);
   cudaFree(h->err);
   delete h;
 }
@@ -165,6 +170,8 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
 
 namespace gptq {
 // Argument checks shared by both checkpoint formats, then the handle and its runtime layout.
+static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split);
+
 static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, const void* scales,
                                  const int32_t* g_idx, int K, int N, int bits, int group_size, gptq_dtype_t dtype,
                                  int fmt, unsigned flags, void* stream, gptq_handle_t* out) {
@@ -209,7 +216,7 @@ static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, con
   s = build_runtime(*h, qweight, qzeros, scales, g_idx, fmt, sf32, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
-  s = gptq_reserve(reinterpret_cast<gptq_handle_t>(h), 32);
+  s = reserve_impl(*h, 32, false);     // the small-M path's permuted-x workspace only
   if (s != GPTQ_OK) { free_handle(h); return s; }
   *out = reinterpret_cast<gptq_handle_t>(h);
   return GPTQ_OK;
@@ -266,12 +273,13 @@ gptq_status_t gptq_repack_fp8(const void* weight, const float* scale_inv, int K,
   return repack_impl(weight, nullptr, scale_inv, nullptr, K, N, 8, 128, dtype, kFmtFp8, 0u, stream, out);
 }
 
-gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
-  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
-  if (max_M < 0) return fail(GPTQ_ERR_INVALID_ARG, "max_M must be >= 0");
-  Handle& h = *reinterpret_cast<Handle*>(hh);
-  if (max_M <= h.reserved_M) return GPTQ_OK;
-  if (!h.identity) {
+}  // extern "C"
+
+namespace gptq {
+// Workspace for calls with M <= max_M: the permuted-x copy (handles whose sorted order is not the
+// identity) and, when with_split, the large-M kernel's K-split partials and tile counters.
+static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
+  if (max_M > h.reserved_M && !h.identity) {
     const size_t bytes = (size_t)max_M * h.Kr * 2;
     void* p = nullptr;
     cudaError_t e = cudaMalloc(&p, bytes);
@@ -280,8 +288,57 @@ gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
     h.xp = p;
     h.xp_bytes = bytes;
   }
-  h.reserved_M = max_M;
+  if (max_M > h.reserved_M) h.reserved_M = max_M;
+  if (with_split && max_M > h.split_reserved_M) {
+    size_t need = 0;
+    int need_cnt = 0;
+    for (int M = 1; M <= max_M; ++M) {
+      const int sp = large_split_for(h, M, SIZE_MAX, INT_MAX);
+      if (sp > 1) {
+        need = std::max(need, (size_t)sp * M * h.Np * sizeof(float));
+        const int bmx = M <= 64 ? 64 : M <= 128 ? 128 : 256;
+        need_cnt = std::max(need_cnt, (M + bmx - 1) / bmx * (h.Np / 128));
+      }
+    }
+    if (need > h.ws_bytes) {
+      void* p = nullptr;
+      cudaError_t e = cudaMalloc(&p, need);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(K-split workspace)");
+      cudaFree(h.ws);
+      h.ws = static_cast<float*>(p);
+      h.ws_bytes = need;
+    }
+    if (need_cnt > h.ws_cnt_n) {
+      int* p = nullptr;
+      cudaError_t e = cudaMalloc(&p, sizeof(int) * (size_t)need_cnt);
+      if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(int) * (size_t)need_cnt);
+      if (e != cudaSuccess) {
+        cudaFree(p);
+        return cuda_fail(e, "cudaMalloc(K-split counters)");
+      }
+      cudaFree(h.ws_cnt);
+      h.ws_cnt = p;
+      h.ws_cnt_n = need_cnt;
+    }
+    h.split_reserved_M = max_M;
+  }
   return GPTQ_OK;
+}
+}  // namespace gptq
+
+extern "C" {
+
+gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  if (max_M < 0) return fail(GPTQ_ERR_INVALID_ARG, "max_M must be >= 0");
+  Handle& h = *reinterpret_cast<Handle*>(hh);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h.device)
+    return fail(GPTQ_ERR_INVALID_ARG, "handle belongs to device " + std::to_string(h.device) + " but device " +
+                                          std::to_string(dev) + " is current");
+  return reserve_impl(h, max_M, true);
 }
 
 gptq_status_t gptq_gemm(gptq_handle_t h, const void* x, void* y, int M, void* stream) {
@@ -298,6 +355,11 @@ int gptq_gemm_launches(gptq_handle_t hh, int M, gptq_path_t path) {
   if (M == 0) return 0;
   if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
   return path == GPTQ_PATH_LARGE_M ? large_m_launches(h, M) : small_m_launches(h, M);
+}
+
+int gptq_gemm_k_splits(gptq_handle_t hh, int M) {
+  if (!hh || M < 0) return -1;
+  return large_split(*reinterpret_cast<const Handle*>(hh), M);
 }
 
 gptq_status_t gptq_destroy(gptq_handle_t hh) {
@@ -339,7 +401,8 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
                        (size_t)h.G * h.Np * (h.fp8 ? 3 : 6) + h.xp_bytes + (h.bias ? sizeof(float) * (size_t)h.Np : 0) +
-                       (h.scale_inv ? sizeof(float) * (size_t)((h.N + 127) / 128) * h.kb : 0);
+                       (h.scale_inv ? sizeof(float) * (size_t)((h.N + 127) / 128) * h.kb : 0) + h.ws_bytes +
+                       sizeof(int) * (size_t)h.ws_cnt_n;
   return GPTQ_OK;
 }
 

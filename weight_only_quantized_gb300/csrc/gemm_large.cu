@@ -95,6 +95,11 @@ struct LargeArgs {
   const float* bias;   // [Np] float32 added to y, or nullptr
   const float* scale_inv;   // FP8 layers: [ceil(N/128)][kb] block factors
   int kb;
+  // K split: CTA z of a tile takes 128-row blocks [NB z / split, NB (z + 1) / split); its fp32 partial
+  // goes to ws[z][m][n] and the last CTA of the tile (counted in cnt) sums the partials in z order
+  int split;
+  float* ws;        // [split][M][Np] (split > 1)
+  int* cnt;         // one counter per (m tile, n tile), zero between calls
 };
 
 __device__ __forceinline__ uint32_t and_or_l(uint32_t a, uint32_t b, uint32_t c) {
@@ -245,8 +250,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m0 = blockIdx.x * BMX, n0 = blockIdx.y * BN;
-  const int nblocks = a.Kr / 128;
-  const int nhalf = 2 * nblocks, nchunks = a.Kr / 32;
+  // this CTA's K range: blocks [kb0, kb1) of 128 sorted rows (all of K without a split)
+  const int z = blockIdx.z;
+  const int kb0 = (int)(((long)(a.Kr / 128) * z) / a.split);
+  const int kb1 = (int)(((long)(a.Kr / 128) * (z + 1)) / a.split);
+  const int nblocks = kb1 - kb0;
+  const int nhalf = 2 * nblocks, nchunks = 4 * nblocks;
+  const int c0 = 4 * kb0;                     // first chunk of the range
 
   const uint32_t xs_s = base_s + S::x, ws_s = base_s + S::w;
   uint8_t* pk = base + S::pk;
@@ -278,11 +288,12 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
                  :: "r"(smem_u32(tmem_slot)), "r"(kCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  for (int i = tid; i < nchunks; i += kThreadsL) cg[i] = __ldg(&a.cgid[i]);
-  // bit j of gmask[w]: chunk 32 w + j is the last chunk of its group (the MMA issuer's schedule)
+  for (int i = tid; i < nchunks; i += kThreadsL) cg[i] = __ldg(&a.cgid[c0 + i]);
+  // bit j of gmask[w]: chunk 32 w + j of the range is the last chunk of its group inside the range
+  // (the MMA issuer's schedule); the range's last chunk always closes one
   for (int w0 = 32 * warp; w0 < nchunks; w0 += kThreadsL) {
     const int c = w0 + lane;
-    const bool end = c < nchunks && (c + 1 == nchunks || __ldg(&a.cgid[c + 1]) != __ldg(&a.cgid[c]));
+    const bool end = c < nchunks && (c + 1 == nchunks || __ldg(&a.cgid[c0 + c + 1]) != __ldg(&a.cgid[c0 + c]));
     const uint32_t m = __ballot_sync(0xffffffffu, end);
     if (lane == 0) gmask[w0 / 32] = m;
   }
@@ -390,9 +401,75 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       }
     }
     if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
-    // y[m][n] for the HC x rows of this half: lanes are consecutive n, so each store is 64 bytes
     uint16_t* y = static_cast<uint16_t*>(a.y);
-    if (n < a.N) {
+    if (a.split > 1) {
+      // this K range's partial, then the tile's counter (every CTA counts once, also after a timeout,
+      // so the counter is back at zero after every call); the CTA that counts last adds the
+      // partials in order of z and stores y.  No CTA waits for another.
+      if (n < a.N) {
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+          const int m = m0 + HC * hs + j;
+          if (m < a.M) a.ws[((size_t)z * a.M + m) * a.Np + n] = acc[j];
+        }
+      }
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" :: "n"(32 * kSc) : "memory");     // the scaler warps only
+      if (sw == 0 && lane == 0) {
+        const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+        const int before = atomicAdd(&a.cnt[tile], 1);
+        const uint32_t last = before == a.split - 1 ? 1u : 0u;
+        if (last) {
+          atomicExch(&a.cnt[tile], 0);
+          __threadfence();
+        }
+        tmem_slot[1] = last;
+      }
+      asm volatile("bar.sync 1, %0;" :: "n"(32 * kSc) : "memory");
+      if (tmem_slot[1] != 0u) {
+        // the tile's rows as float4 runs of four columns, spread over the scaler threads, every
+        // partial (this CTA's included) read back from L2 in order of z: the same sum whichever CTA
+        // of the tile is last; four runs per thread in flight
+        const int rows = min(BMX, a.M - m0);
+        const int runs = rows * (BN / 4);
+        for (int i0 = 32 * sw + lane; i0 < runs; i0 += 4 * 32 * kSc) {
+          float4 t[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) t[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int zz = 0; zz < a.split; ++zz) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = i0 + u * 32 * kSc;
+              if (i < runs) {
+                const int m = m0 + i / (BN / 4), nn = n0 + 4 * (i % (BN / 4));
+                if (nn < a.N) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws + ((size_t)zz * a.M + m) * a.Np + nn));
+                  t[u].x += v.x; t[u].y += v.y; t[u].z += v.z; t[u].w += v.w;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 32 * kSc;
+            if (i < runs) {
+              const int m = m0 + i / (BN / 4), nn = n0 + 4 * (i % (BN / 4));
+              if (nn < a.N) {
+                if (a.bias) {
+                  const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + nn));
+                  t[u].x += b.x; t[u].y += b.y; t[u].z += b.z; t[u].w += b.w;
+                }
+                uint2 o;
+                o.x = (uint32_t)to_bits<T>(t[u].x) | ((uint32_t)to_bits<T>(t[u].y) << 16);
+                o.y = (uint32_t)to_bits<T>(t[u].z) | ((uint32_t)to_bits<T>(t[u].w) << 16);
+                *reinterpret_cast<uint2*>(y + (size_t)m * a.N + nn) = o;
+              }
+            }
+          }
+        }
+      }
+    } else if (n < a.N) {
+      // y[m][n] for the HC x rows of this half: lanes are consecutive n, so each store is 64 bytes
       if (a.bias) {
         const float b = __ldg(a.bias + n);
 #pragma unroll
@@ -415,7 +492,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
           const int xs = i % XS;
           if (i >= XS && !mbar_wait(x_empty(xs), ((i / XS) - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(x_full(xs), XB);
-          tma_load_2d(xs_s + xs * XB, &tmap_x, i * HK, m0, x_full(xs));
+          tma_load_2d(xs_s + xs * XB, &tmap_x, (2 * kb0 + i) * HK, m0, x_full(xs));
           ++x_issued;
         }
         // every issued copy must land before the CTA may exit
@@ -433,7 +510,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
           const int ps = blk % PS;
           if (blk >= PS && !mbar_wait(pk_empty(ps), ((blk / PS) - 1) & 1)) { ok = false; break; }
           mbar_arrive_expect_tx(pk_full(ps), FP8 ? (uint32_t)PK_BYTES<BITS> : (uint32_t)PKB);   // FP8: no zeros
-          const uint8_t* src = a.wr + ((size_t)blk * BITS * a.Np + n0) * 16;
+          const uint8_t* src = a.wr + ((size_t)(kb0 + blk) * BITS * a.Np + n0) * 16;
   #pragma unroll
           for (int v = 0; v < BITS; ++v)
             bulk_g2s(smem_u32(pk + ps * PKB + v * BN * 16), src + (size_t)v * a.Np * 16, BN * 16, pk_full(ps));
@@ -578,6 +655,45 @@ template <int BITS, int BMX> size_t large_smem_bytes(int Kr) {
 // x rows per tile: the smallest of 64, 128, 256 that covers M (and 256 above it)
 inline int bmx_for(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
+}  // namespace
+
+// K split of the large-M kernel at M: the number of ranges s (1 .. 8, each of at least 8 blocks)
+// with the smallest estimated time waves(s) * (t0 + t_k / s) + t_red(s), where waves(s) =
+// ceil(tiles s / SMs), t_k is one CTA's pass over all of K (~700 / 800 / 950 cycles per 64-k stage
+// at 64 / 128 / 256 x rows, at 1.9 GHz), t0 ~3 us a CTA's fixed start and drain, and t_red the last
+// CTA's read of the s partials of its tile at ~130 GB/s -- a grid with fewer tiles than SMs, or a
+// mostly empty last wave, gains -- and whose partials fit kSplitWsCap bytes.  `avail` and `cnt`
+// (workspace bytes and counters on hand) bound it further; pass SIZE_MAX / INT_MAX to ask what M
+// would take.
+int large_split_for(const Handle& h, int M, size_t avail, int cnt) {
+  if (M <= 0) return 1;
+  const int bmx = bmx_for(M);
+  const long tiles = (long)((M + bmx - 1) / bmx) * (h.Np / BN);
+  const int nb = h.Kr / 128;
+  const double stage_cycles = bmx == 64 ? 700.0 : bmx == 128 ? 800.0 : 950.0;
+  const double t_k = (h.Kr / 64) * stage_cycles / 1.9e3;          // us
+  const double t0 = 3.0;
+  auto cost = [&](int s) {
+    const double waves = (double)((tiles * s + h.sm_count - 1) / h.sm_count);
+    const double red = s > 1 ? (double)s * std::min(M, bmx) * BN * 4 / 130e3 : 0.0;
+    return waves * (t0 + t_k / s) + red;
+  };
+  int best = 1;
+  double best_cost = cost(1);
+  for (int s = 2; s <= 8 && nb / s >= 8; ++s) {
+    const size_t bytes = (size_t)s * M * h.Np * sizeof(float);
+    if (cost(s) < best_cost * 0.95 && bytes <= kSplitWsCap && bytes <= avail && tiles <= cnt) {
+      best = s;
+      best_cost = cost(s);
+    }
+  }
+  return best;
+}
+
+int large_split(const Handle& h, int M) { return large_split_for(h, M, h.ws_bytes, h.ws_cnt_n); }
+
+namespace {
+
 template <typename T, int BITS, int BMX, bool FP8>
 cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
   const size_t smem = large_smem_bytes<BITS, BMX>(h.Kr);
@@ -592,10 +708,11 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  const int split = large_split(h, M);
   LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff, h.has_bias ? h.bias : nullptr,
-                 h.scale_inv, h.kb};
+                 h.scale_inv, h.kb, split, h.ws, h.ws_cnt};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, 1);     // consecutive CTAs share a weight tile
+  cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, split);  // consecutive CTAs share a weight tile
   cfg.blockDim = dim3(kThreadsL);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -34,6 +34,12 @@ struct Handle {
   uint8_t* z_r = nullptr;    // [G][Np] stored zero field (GPTQ: zero - 1; AWQ: the zero itself)
   int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ v1 fields, 0 for gptq_v2 and AWQ
   float* bias = nullptr;     // [Np] float32 bias added to y (pad columns 0), allocated by gptq_set_bias
+  // K-split workspace of the large-M kernel (sized by gptq_reserve)
+  float* ws = nullptr;       // fp32 partials [split][M][Np]
+  size_t ws_bytes = 0;
+  int* ws_cnt = nullptr;     // one counter per (m tile, n tile), zero between calls
+  int ws_cnt_n = 0;
+  int split_reserved_M = 0;  // gptq_reserve sized the split workspace for M up to this
   // FP8 block-scaled layers (codes are e4m3 bytes; no zeros; s_r and z_r are not allocated)
   int fp8 = 0;
   float* scale_inv = nullptr;   // [ceil(N/128)][kb] float32, one factor per 128 x 128 block
@@ -104,6 +110,12 @@ enum Format { kFmtGptq = 0, kFmtAwq = 1, kFmtFp8 = 2 };
 
 // bias[n] -> float32 [Np] (kind 0 fp16, 1 bf16, 2 float32; pad columns 0), enqueued on st.
 cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst, cudaStream_t st);
+
+// Large-M K split: ranges for M given the workspace on hand (1 = none); the workspace bytes a split
+// may take at most.
+constexpr size_t kSplitWsCap = 64ull << 20;
+int large_split_for(const Handle& h, int M, size_t avail, int cnt);
+int large_split(const Handle& h, int M);
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
