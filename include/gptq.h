@@ -216,9 +216,10 @@ gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gpt
  * argument.  Host only. */
 int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
 
-/* Number of K ranges the large-M kernel splits a call at this M into (1 = none; more only where
- * gptq_reserve covered M), or -1 on a bad argument.  Host only. */
-int gptq_gemm_k_splits(gptq_handle_t h, int M);
+/* Number of K ranges a gptq_gemm_path call at this M is split into (1 = none): the large-M kernel
+ * splits grids that would leave SMs idle, where gptq_reserve covered M; the small-M kernel never
+ * splits.  -1 on a bad argument.  Host only. */
+int gptq_gemm_k_splits(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Free the handle and everything it owns.  Waits for the device to finish using it
  * (cudaDeviceSynchronize on the handle's device).  NULL is accepted. */

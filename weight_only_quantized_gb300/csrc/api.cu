@@ -300,6 +300,7 @@ static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
         need_cnt = std::max(need_cnt, (M + bmx - 1) / bmx * (h.Np / 128));
       }
     }
+    bool grew = false;
     if (need > h.ws_bytes) {
       void* p = nullptr;
       cudaError_t e = cudaMalloc(&p, need);
@@ -307,6 +308,7 @@ static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
       cudaFree(h.ws);
       h.ws = static_cast<float*>(p);
       h.ws_bytes = need;
+      grew = true;
     }
     if (need_cnt > h.ws_cnt_n) {
       int* p = nullptr;
@@ -319,6 +321,11 @@ static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
       cudaFree(h.ws_cnt);
       h.ws_cnt = p;
       h.ws_cnt_n = need_cnt;
+      grew = true;
+    }
+    if (grew) {   // cached launch plans were made without this workspace
+      std::lock_guard<std::mutex> lock(h.plan_mu);
+      h.plans.clear();
     }
     h.split_reserved_M = max_M;
   }
@@ -357,9 +364,12 @@ int gptq_gemm_launches(gptq_handle_t hh, int M, gptq_path_t path) {
   return path == GPTQ_PATH_LARGE_M ? large_m_launches(h, M) : small_m_launches(h, M);
 }
 
-int gptq_gemm_k_splits(gptq_handle_t hh, int M) {
+int gptq_gemm_k_splits(gptq_handle_t hh, int M, gptq_path_t path) {
   if (!hh || M < 0) return -1;
-  return large_split(*reinterpret_cast<const Handle*>(hh), M);
+  if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M) return -1;
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  return path == GPTQ_PATH_LARGE_M ? large_split(h, M) : 1;     // the small-M kernel walks all of K
 }
 
 gptq_status_t gptq_destroy(gptq_handle_t hh) {

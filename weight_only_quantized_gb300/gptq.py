@@ -49,7 +49,7 @@ SIGNATURES = {
     "gptq_gemm": (_I, [_P, _P, _P, _I, _P]),
     "gptq_gemm_path": (_I, [_P, _P, _P, _I, _I, _P]),
     "gptq_gemm_launches": (_I, [_P, _I, _I]),
-    "gptq_gemm_k_splits": (_I, [_P, _I]),
+    "gptq_gemm_k_splits": (_I, [_P, _I, _I]),
     "gptq_destroy": (_I, [_P]),
     "gptq_get_info": (_I, [_P, C.POINTER(GptqInfo)]),
     "gptq_copy_runtime": (_I, [_P, _P, _P, _P, _P, _P]),
@@ -246,8 +246,8 @@ def gptq_gemm_launches(h: Handle, M: int, path: int = PATH_AUTO) -> int:
     return lib().gptq_gemm_launches(h.ptr, M, path)
 
 
-def gptq_gemm_k_splits(h: Handle, M: int) -> int:
-    return lib().gptq_gemm_k_splits(h.ptr, M)
+def gptq_gemm_k_splits(h: Handle, M: int, path: int = PATH_LARGE_M) -> int:
+    return lib().gptq_gemm_k_splits(h.ptr, M, path)
 
 
 def gptq_destroy(h: Handle):
