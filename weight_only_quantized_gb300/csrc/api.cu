@@ -296,8 +296,7 @@ static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
       const int sp = large_split_for(h, M, SIZE_MAX, INT_MAX);
       if (sp > 1) {
         need = std::max(need, (size_t)sp * M * h.Np * sizeof(float));
-        const int bmx = M <= 64 ? 64 : M <= 128 ? 128 : 256;
-        need_cnt = std::max(need_cnt, (M + bmx - 1) / bmx * (h.Np / 128));
+        need_cnt = std::max(need_cnt, large_tile_count(h, M));
       }
     }
     bool grew = false;

@@ -655,6 +655,22 @@ template <int BITS, int BMX> size_t large_smem_bytes(int Kr) {
 // x rows per tile: the smallest of 64, 128, 256 that covers M (and 256 above it)
 inline int bmx_for(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 
+template <int BITS> size_t smem_at(int bmx, int Kr) {
+  return bmx == 64 ? large_smem_bytes<BITS, 64>(Kr) : bmx == 128 ? large_smem_bytes<BITS, 128>(Kr)
+                                                                  : large_smem_bytes<BITS, 256>(Kr);
+}
+inline size_t smem_bits(int bits, int bmx, int Kr) {
+  return bits == 2 ? smem_at<2>(bmx, Kr) : bits == 3 ? smem_at<3>(bmx, Kr) : bits == 4 ? smem_at<4>(bmx, Kr)
+                                                                                    : smem_at<8>(bmx, Kr);
+}
+// The x tile used at M: bmx_for(M), narrowed while the chunk tables of a very long K leave its
+// rings no room (the narrower tiles have smaller x rings); 0 if even 64 rows do not fit.
+inline int large_bmx(const Handle& h, int M) {
+  int bmx = bmx_for(M);
+  while (bmx > 64 && smem_bits(h.bits, bmx, h.Kr) > 227 * 1024) bmx /= 2;
+  return smem_bits(h.bits, bmx, h.Kr) <= 227 * 1024 ? bmx : 0;
+}
+
 }  // namespace
 
 // K split of the large-M kernel at M: the number of ranges s (1 .. 8, each of at least 8 blocks)
@@ -666,8 +682,8 @@ inline int bmx_for(int M) { return M <= 64 ? 64 : M <= 128 ? 128 : 256; }
 // (workspace bytes and counters on hand) bound it further; pass SIZE_MAX / INT_MAX to ask what M
 // would take.
 int large_split_for(const Handle& h, int M, size_t avail, int cnt) {
-  if (M <= 0) return 1;
-  const int bmx = bmx_for(M);
+  const int bmx = M > 0 ? large_bmx(h, M) : 0;
+  if (bmx == 0) return 1;
   const long tiles = (long)((M + bmx - 1) / bmx) * (h.Np / BN);
   const int nb = h.Kr / 128;
   const double stage_cycles = bmx == 64 ? 700.0 : bmx == 128 ? 800.0 : 950.0;
@@ -691,6 +707,11 @@ int large_split_for(const Handle& h, int M, size_t avail, int cnt) {
 }
 
 int large_split(const Handle& h, int M) { return large_split_for(h, M, h.ws_bytes, h.ws_cnt_n); }
+
+int large_tile_count(const Handle& h, int M) {
+  const int bmx = M > 0 ? large_bmx(h, M) : 0;
+  return bmx ? (M + bmx - 1) / bmx * (h.Np / BN) : 0;
+}
 
 namespace {
 
@@ -726,7 +747,7 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
 
 template <typename T, int BITS, bool FP8 = false>
 cudaError_t launch_tb(const Handle& h, const CUtensorMap& map, void* y, int M, cudaStream_t st) {
-  switch (bmx_for(M)) {
+  switch (large_bmx(h, M)) {
     case 64: return launch_tbm<T, BITS, 64, FP8>(h, map, y, M, st);
     case 128: return launch_tbm<T, BITS, 128, FP8>(h, map, y, M, st);
     default: return launch_tbm<T, BITS, 256, FP8>(h, map, y, M, st);
@@ -763,7 +784,8 @@ bool large_m_available() { return true; }
 int large_m_launches(const Handle& h, int M) { return M > 0 ? (h.identity ? 1 : 2) : 0; }
 
 cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  if (large_smem_bytes<8, 256>(h.Kr) > 227 * 1024) return cudaErrorInvalidConfiguration;
+  const int bmx = large_bmx(h, M);
+  if (bmx == 0) return cudaErrorInvalidConfiguration;
   const void* src = x;
   int kdim = h.K;
   if (!h.identity) {
@@ -779,7 +801,7 @@ cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cu
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)kdim, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)kdim * 2};
-  const cuuint32_t box[2] = {HK, (cuuint32_t)bmx_for(M)};
+  const cuuint32_t box[2] = {HK, (cuuint32_t)bmx};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = h.dtype == GPTQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (enc(&map, dt, 2, const_cast<void*>(src), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -266,6 +266,8 @@ struct SmallArgs {
                     // start is not hidden behind the previous call); 0: every thread loads it at start
   int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields, stored minus one; 0: gptq_v2, AWQ)
   const float* bias;   // [Np] float32 added to y, or nullptr
+  int xs_on;        // 1: the x sums of the CTA's first tile are kept for its later tiles (a table of
+                    // NB * 8 * MT8 floats); 0 when shared memory is short (very long K)
 };
 
 template <int CW>
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt) {
                   xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
-                  if (kFZ && g == 0)
+                  if (kFZ && g == 0 && a.xs_on)
                     *reinterpret_cast<float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t) = xsv[mt];
                 }
               }
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           }
         }
       };
-      if (ti > T0) run_blocks(std::true_type{});
+      if (ti > T0 && a.xs_on) run_blocks(std::true_type{});
       else run_blocks(std::false_type{});
       s_base += nst;
       __syncwarp();
@@ -729,11 +731,14 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
   int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw,
-      gather, o_pm, o_raw, cg_async;
+      gather, o_pm, o_raw, cg_async, xs_on;
 };
 
 // Layout for codes of `bits` bits and MT8 m-tiles; with_gather adds the perm copy.
-bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p) {
+// level 0: the preferred layout; level >= 1 (when that does not fit, e.g. K of 64 Ki and more, whose
+// per-group header and per-block tables grow with K): 8 consumer warps, no x-sum table, and K
+// panels of at most NB >> (level - 1) blocks.
+bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p, int level = 0) {
   const int NB = h.Kr / 128;
   p.ntiles = (h.N + kTileN - 1) / kTileN;
   p.grid = std::min(p.ntiles, h.sm_count);
@@ -744,14 +749,20 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   // call's CTA can start streaming beside it; a long one takes the whole SM, a deeper ring and
   // (at M <= 8) 16 consumer warps.
   const bool short_cta = x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3;
-  p.cw = (mt8 == 1 && !short_cta) ? 16 : 8;
-  if (x_all <= kXSingle) {
+  p.cw = (mt8 == 1 && !short_cta && level == 0) ? 16 : 8;
+  p.xs_on = level == 0 ? 1 : 0;
+  if (level == 0 && x_all <= kXSingle) {
     p.single = 1;
     p.pb = NB;
     if (short_cta) target = kSmemHalf;
-  } else {
+  } else if (level == 0) {
     p.single = 0;
     p.pb = std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB);
+  } else {
+    const int cap = std::max(kSPB, (NB >> (level - 1)) / kSPB * kSPB);
+    p.pb = std::min(cap, std::max(kSPB, (kXPanel / M - 64) / 256 / kSPB * kSPB));
+    p.single = p.pb >= NB ? 1 : 0;
+    if (p.single) p.pb = NB;
   }
   p.gather = (with_gather && p.single) ? 1 : 0;
   p.npanel = (NB + p.pb - 1) / p.pb;
@@ -765,7 +776,7 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const int zs_bytes = 2 * p.span_max * kZsRow;
   const int red_bytes = p.cw * mt8 * 8 * (kTileN + 4) * 4;
   const int cg_bytes = (NB * 4 * 4 + 15) / 16 * 16;
-  const int xs_bytes = NB * 8 * mt8 * 4;      // x sums per block, reused by every tile after the first
+  const int xs_bytes = p.xs_on ? NB * 8 * mt8 * 4 : 0;   // x sums per block, reused by the later tiles
   const int pm_bytes = p.gather ? h.Kr * 4 : 0;
   const int raw_bytes = p.gather ? M * h.K * 2 : 0;
   const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + 5 * 8 + 16;
@@ -783,6 +794,10 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   p.lg_rd = 0;
   while ((2 << p.lg_rd) <= rd) ++p.lg_rd;     // largest power of two <= rd
   const int rdp = 1 << p.lg_rd;
+  // A consumer warp's consecutive stages are cw / kSPB apart.  A parity wait on a slot tells apart
+  // only the slot's current and previous phase, so the ring must hold at least that many stages
+  // (else a warp would wait two phases ahead on the same slot and read a stale stage).
+  if (rdp * kSPB < p.cw) return false;
   p.o_x = rdp * SB;
   p.o_zs = p.o_x + (x_bytes + 15) / 16 * 16;
   p.o_red = p.o_zs + zs_bytes;
@@ -800,7 +815,9 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
 bool make_plan(const Handle& h, int M, SmallPlan& p) {
   const int mt8 = M <= 8 ? 1 : M <= 16 ? 2 : 4;
   if (!h.identity && !h.fp8 && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
-  return plan_layout(h, M, h.bits, mt8, false, p);
+  for (int level = 0; level <= 12; ++level)
+    if (plan_layout(h, M, h.bits, mt8, false, p, level)) return true;
+  return false;
 }
 
 template <typename T, int BITS, int MT8, bool FP8>
@@ -850,7 +867,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
-                 h.zoff, h.has_bias ? h.bias : nullptr};
+                 h.zoff, h.has_bias ? h.bias : nullptr, p.xs_on};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());

@@ -116,6 +116,7 @@ cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst
 constexpr size_t kSplitWsCap = 64ull << 20;
 int large_split_for(const Handle& h, int M, size_t avail, int cnt);
 int large_split(const Handle& h, int M);
+int large_tile_count(const Handle& h, int M);   // output tiles (x tile x 128 weight rows) at M
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
