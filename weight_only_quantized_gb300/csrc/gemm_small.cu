@@ -266,8 +266,6 @@ struct SmallArgs {
                     // start is not hidden behind the previous call); 0: every thread loads it at start
   int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields, stored minus one; 0: gptq_v2, AWQ)
   const float* bias;   // [Np] float32 added to y, or nullptr
-  int xs_on;        // 1: the x sums of the CTA's first tile are kept for its later tiles (a table of
-                    // NB * 8 * MT8 floats); 0 when shared memory is short (very long K)
 };
 
 template <int CW>
@@ -275,7 +273,9 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" :: "n"(CW * 32) : "memory");
 }
 
-template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8>
+// XS: the x sums of the CTA's first tile are kept (a table of NB * 8 * MT8 floats) for its later
+// tiles; false only in the layouts for very long K, where shared memory cannot hold the table.
+template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8, bool XS = true>
 __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
   static_assert(!FP8 || (BITS == 8 && !GATHER), "FP8 layers: 8-bit layout, x staged without gather");
   // the zero fold applies to integer codes; FP8 weights are their own values
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
                 for (int mt = 0; mt < MT8; ++mt) {
                   xsv[mt] = make_float2(xsp[mt][0], xsp[mt][1]);
-                  if (kFZ && g == 0 && a.xs_on)
+                  if (kFZ && XS && g == 0)
                     *reinterpret_cast<float2*>(xsb + (size_t)b * (8 * MT8) + 8 * mt + 2 * t) = xsv[mt];
                 }
               }
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           }
         }
       };
-      if (ti > T0 && a.xs_on) run_blocks(std::true_type{});
+      if (XS && ti > T0) run_blocks(std::true_type{});
       else run_blocks(std::false_type{});
       s_base += nst;
       __syncwarp();
@@ -830,6 +830,8 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
     if (it == h.plans.end()) {
       if (!make_plan(h, M, p)) return cudaErrorInvalidConfiguration;
       cudaError_t e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false, FP8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if constexpr (MT8 == 1) {
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if constexpr (!FP8) {
@@ -867,7 +869,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
-                 h.zoff, h.has_bias ? h.bias : nullptr, p.xs_on};
+                 h.zoff, h.has_bias ? h.bias : nullptr};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
@@ -875,6 +877,8 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (!p.xs_on)   // the long-K layouts: 8 consumer warps, no gather, no x-sum table
+    return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8, false>, args, h.wr_map);
   if constexpr (MT8 == 1) {
     if constexpr (!FP8) {
       if (p.gather)
