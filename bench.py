@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -56,13 +57,21 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def code_sha256(text: str) -> str:
+    """SHA-256 of a source with its comments removed and whitespace collapsed: edits to comments do
+    not change the kernel the counters were taken on."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
 def traffic_record(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's code is unchanged."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "weight_only_quantized_gb300", "csrc", kernel_file), "rb").read()
-        if rec.get(kernel_file, {}).get("source_sha256") == hashlib.sha256(src).hexdigest():
+        src = open(os.path.join(ROOT, "weight_only_quantized_gb300", "csrc", kernel_file)).read()
+        if rec.get(kernel_file, {}).get("code_sha256") == code_sha256(src):
             return rec[kernel_file]
     except Exception:
         pass

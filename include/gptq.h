@@ -9,6 +9,10 @@
  *   - inference.shantanugoel.com ch. 39 "Quantized checkpoints", section "The format"
  *     (qweight int32 [K*bits/32, N], codes along K, low bits first; qzeros int32
  *     [G, N*bits/32], zeros along N, stored minus one; scales [G, N]; g_idx int32 [K]).
+ * The same handle and GEMM serve the neighbouring formats of that chapter: gptq_v2 zero fields
+ * and float32 scales (gptq_repack_ex), AutoAWQ GEMM checkpoints (section "AWQ",
+ * gptq_repack_awq) and FP8 block-scaled W8A16 layers (section "FP8 checkpoints",
+ * gptq_repack_fp8), with an optional bias (gptq_set_bias).
  * Weights stay packed from HBM until they reach registers or shared memory; the dense W is
  * never written to memory (mlinterviewnotes "Formats and kernels: FP8, INT8, INT4, Marlin,
  * Machete", opening section).

@@ -31,6 +31,11 @@
 //    S += scale[g][n] * P in registers, release the buffer.  At the end they round S to the output
 //    type and store y.  setmaxnreg gives them 184 registers a thread and the other warps 72.
 // Act-order handles first gather x into the handle's workspace in sorted k order (one extra launch).
+// FP8 block-scaled layers (template FP8): the dequantisers convert e4m3 pairs (fp8_pair) with no
+// zero, and the scalers multiply by the CTA's 128 x 128 block factor.
+// K split (grids that would leave SMs idle): blockIdx.z takes a range of 128-row blocks, the
+// partials go to an fp32 workspace, and the last CTA of each tile (an atomic counter, no waiting)
+// sums them in range order and stores y.  A very long K narrows the x tile until the tables fit.
 // Every wait is bounded; a timeout sets the handle's error word and the CTA drains and exits.
 #include "internal.cuh"
 

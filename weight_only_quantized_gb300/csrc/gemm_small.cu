@@ -29,6 +29,11 @@
 //    per pair of codes; fp16 1024 + q, bf16 128 + q) and the zero comes out once per block in fp32
 //    against the sum of x; the group scale multiplies that fp32 partial sum.  8-bit codes with bf16
 //    go through the 2^23 fp32 magic, because bf16 holds 128 + q exactly only for q < 128.
+//  * FP8 block-scaled layers (template FP8): the e4m3 bytes of a pair sit side by side in the
+//    layout, one cvt.rn.f16x2.e4m3x2 makes the operand (plus an exact shift and multiply for bf16),
+//    no zero fold, and the 128 x 128 block's factor multiplies the partial sum.
+//  * Very long K (template XS false): when the per-block x-sum table does not fit shared memory the
+//    planner takes 8 consumer warps, smaller K panels and recomputes the x sums for every tile.
 //  * Every wait is bounded; a timeout sets the handle's error word, and the CTA drains its copies
 //    and exits.
 #include "internal.cuh"
