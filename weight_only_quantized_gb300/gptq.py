@@ -314,19 +314,13 @@ class GptqLinear:
     @classmethod
     def from_fp8(cls, weight, scale_inv, dtype: torch.dtype, stream=None, *, bias=None) -> "GptqLinear":
         """The same layer object built from an FP8 block-scaled checkpoint (W8A16)."""
-        h = gptq_repack_fp8(weight, scale_inv, dtype, stream)
-        obj = cls.__new__(cls)
-        obj.handle = h
-        info = gptq_get_info(h)
-        obj.K, obj.N, obj.dtype = info.K, info.N, dtype
-        if bias is not None:
-            gptq_set_bias(h, bias, stream)
-        return obj
+        return cls(None, None, None, None, 8, 128, stream, bias=bias,
+                   _handle=gptq_repack_fp8(weight, scale_inv, dtype, stream))
 
     @classmethod
     def from_awq(cls, qweight, qzeros, scales, group_size: int, stream=None, *, bias=None) -> "GptqLinear":
         """The same layer object built from an AutoAWQ GEMM checkpoint."""
-        return cls(None, None, scales, None, 4, group_size, bias=bias,
+        return cls(None, None, scales, None, 4, group_size, stream, bias=bias,
                    _handle=gptq_repack_awq(qweight, qzeros, scales, group_size, stream))
 
     def __call__(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
