@@ -21,7 +21,6 @@ permutation, x.  Everything is drawn on the CPU with torch.Generator.
 from __future__ import annotations
 
 import dataclasses
-import math
 from typing import Optional
 
 import torch
