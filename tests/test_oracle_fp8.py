@@ -96,3 +96,18 @@ def test_fp8_layout_decodes_back(K, N):
     real = perm >= 0
     ref[np.ix_(real, np.arange(N))] = w[:, perm[real]].T
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_fp8_linear_matches_a_product_built_from_torch_float8(dtype):
+    """The whole FP8 path against one built only from torch: float8_e4m3fn decoding of the bytes,
+    the 128 x 128 factors expanded by repeat_interleave, float32 products, a float64 matmul."""
+    K, N, M = 384, 160, 3
+    ck = synth.make_fp8_checkpoint(K, N, dtype, seed=21)
+    x = synth.make_x(M, K, dtype, seed=22)
+    w = ck.weight.view(torch.float8_e4m3fn).float()
+    s = ck.scale_inv.repeat_interleave(128, 0)[:N].repeat_interleave(128, 1)[:, :K]
+    W = (w * s).double()                                      # float32 products, as dequantize_blocks
+    ref = (x.double() @ W.T).numpy()
+    y = oracle.fp8_linear(ck.weight, ck.scale_inv, dtype, x)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
