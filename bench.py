@@ -2,18 +2,22 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
-One step is one gptq_gemm call (the whole per-call hot path: activation gather, packed-weight
-stream, dequant, MMA, split-K reduction, y store) on the Llama-3-8B-shaped decode layer
-(K=4096, N=14336, 4-bit, group 128, symmetric zero 8, bf16) at M=1.  Successive steps use
-successive weight sets of a 16-layer resident stack, so the working set (489 MB) is larger
-than L2 and no step reads weights another step left in L2.  Inputs are synthetic and seeded.
+One step is one gptq_gemm call (the whole per-call hot path: activation permute, packed-weight
+stream, dequant, MMA, reduction, y store) on the Llama-3-70B gate_proj layer (K=8192, N=28672,
+4-bit, group 128, act-order, asymmetric zeros, fp16) at M=1, the largest M=1 configuration.
+Successive steps use successive weight sets of an 8-layer resident stack, so the working set
+(977 MB) is larger than L2 and no step reads weights another step left in L2.  Inputs are
+synthetic and seeded.
 
-value  = algorithmic bytes moved per call (packed weights + scales + packed zeros + x + y)
-         divided by the time per call, summed over ranks (one replica per GPU).
+value  = algorithmic bytes moved per call (packed weights + scales + packed zeros + perm + x + y)
+         divided by the time per call, summed over ranks (one replica per GPU).  The time per call
+         is the median over repeated replays of a CUDA graph of `steps` calls, replayed until at
+         least 200 ms have been timed.
 e2e    = the same metric through the public API with host buffers: pinned x copied to the
          device, gptq_gemm, y copied back, every step.
-Also reported (rank 0): the 70B gate_proj layer at M=1 and the prefill layer at M=4096, and the
-oracle timed on the host cores (cpu_baseline).
+Also reported (rank 0): the Llama-3-8B decode layer at M=1 (decode_m1) and the prefill layer at
+M=4096 (prefill_m4096) as top-level keys, more M values and formats under detail, and the oracle
+timed on the host cores (cpu_baseline).
 
 --impl reference times the CPU oracle (the only reference this build has: the pages publish
 no runnable code) on a bounded sample of the same workload.
@@ -34,9 +38,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "llama3-8b-decode-4096x14336-b4g128-sym"
+WORKLOAD = "llama3-70b-gate-8192x28672-b4g128-descact"
+DECODE = "llama3-8b-decode-4096x14336-b4g128-sym"
+PREFILL = "prefill-8192x28672-b4g128"
 METRIC = "GPTQ W4A16 GEMM µs/call, HBM GB/s (M=1), TFLOP/s (M=4096), % roofline"
-LAYERS = 16
+LAYERS = 8
+MIN_TIMED_S = 0.2
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -65,14 +72,15 @@ def code_sha256(text: str) -> str:
     return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
 
 
-def traffic_record(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's code is unchanged."""
+def traffic_record(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this workload, if the
+    kernel's code is unchanged since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)
+            rec = json.load(f).get(f"{kernel_file}:{workload}", {})
         src = open(os.path.join(ROOT, "weight_only_quantized_gb300", "csrc", kernel_file)).read()
-        if rec.get(kernel_file, {}).get("code_sha256") == code_sha256(src):
-            return rec[kernel_file]
+        if rec.get("code_sha256") == code_sha256(src):
+            return rec
     except Exception:
         pass
     return None
@@ -203,11 +211,11 @@ def run_reference(args, ws, rank):
     rng = np.random.default_rng(0)
     for _ in range(max(0, args.warmup - 1)):
         c = np.sort(rng.choice(spec.N, cols, replace=False)).astype(np.int32)
-        oracle.linear(ck.qweight, ck.qzeros, ck.scales, None, spec.bits, spec.group_size, spec.dtype, x, None, c)
+        oracle.linear(ck.qweight, ck.qzeros, ck.scales, ck.g_idx, spec.bits, spec.group_size, spec.dtype, x, None, c)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         c = np.sort(rng.choice(spec.N, cols, replace=False)).astype(np.int32)
-        oracle.linear(ck.qweight, ck.qzeros, ck.scales, None, spec.bits, spec.group_size, spec.dtype, x, None, c)
+        oracle.linear(ck.qweight, ck.qzeros, ck.scales, ck.g_idx, spec.bits, spec.group_size, spec.dtype, x, None, c)
     dt = time.perf_counter() - t0
     frac = cols / spec.N
     value = b_alg(spec, M) * frac * args.steps / dt / 1e9
@@ -216,7 +224,8 @@ def run_reference(args, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "K": spec.K, "N": spec.N, "bits": spec.bits,
-                       "group_size": spec.group_size, "parallelism": "rank 0 only (host cores)"},
+                       "group_size": spec.group_size, "act_order": spec.desc_act,
+                       "parallelism": "rank 0 only (host cores)"},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -225,26 +234,33 @@ def run_reference(args, ws, rank):
 
 
 # ----------------------------------------------------------------------------- native arm
-def make_layers(spec, count, seed0=0):
+def make_layers(spec, count, seed0=0, distinct=False):
+    """`count` resident handles of the layer: repacks of one seeded checkpoint (distinct=False; the
+    handles are separate device copies, so each call streams its own weights from HBM) or of
+    `count` checkpoints with successive seeds."""
     import torch
     from weight_only_quantized_gb300 import gptq, synth
     hs, cks = [], []
+    dev = None
     for i in range(count):
-        ck = synth.make_checkpoint(spec, seed=seed0 + i)
-        h = gptq.gptq_repack(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(),
-                             None if ck.g_idx is None else ck.g_idx.cuda(), spec.bits, spec.group_size)
-        hs.append(h)
-        cks.append(ck)
+        if distinct or i == 0:
+            ck = synth.make_checkpoint(spec, seed=seed0 + i)
+            dev = [t.cuda() if t is not None else None for t in (ck.qweight, ck.qzeros, ck.scales, ck.g_idx)]
+            cks.append(ck)
+        hs.append(gptq.gptq_repack(dev[0], dev[1], dev[2], dev[3], spec.bits, spec.group_size))
+    del dev
     torch.cuda.synchronize()
     return hs, cks
 
 
-def time_calls(hs, xs, ys, M, steps, warmup, graph=True):
-    """Average per-call device time (s) of `steps` calls rotating over the handles.
+def time_calls(hs, xs, ys, M, steps, warmup, graph=True, min_total_s=MIN_TIMED_S, min_reps=5):
+    """Per-call device time (s) of `steps` calls rotating over the handles.
 
     graph=True: the `steps` calls are captured once into a CUDA graph (how a decode step is
-    deployed) and the timed region is one replay, bracketed by CUDA events on the replay stream.
-    graph=False: eager launches from the host, events around the loop."""
+    deployed); the graph is replayed until at least `min_total_s` of replays (and at least five)
+    have been timed, each replay bracketed by CUDA events on the replay stream, and the median
+    replay time / steps is returned.  graph=False: eager launches from the host, events around the
+    loop, repeated the same way.  (min_total_s = 0, min_reps = 1: exactly `steps` timed calls.)"""
     import torch
     from weight_only_quantized_gb300 import gptq
     n = len(hs)
@@ -253,6 +269,7 @@ def time_calls(hs, xs, ys, M, steps, warmup, graph=True):
         gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M, st)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g = None
     if graph:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -261,19 +278,35 @@ def time_calls(hs, xs, ys, M, steps, warmup, graph=True):
         torch.cuda.synchronize()
         g.replay()                      # untimed replay: graph upload and first-touch effects
         torch.cuda.synchronize()
-        st = torch.cuda.current_stream()
+    st = torch.cuda.current_stream()
+    times, total = [], 0.0
+    while total < min_total_s or len(times) < min_reps:
         t0.record(st)
-        g.replay()
+        if graph:
+            g.replay()
+        else:
+            for i in range(steps):
+                gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M, st)
         t1.record(st)
         torch.cuda.synchronize()
-        del g
-    else:
-        t0.record(st)
-        for i in range(steps):
-            gptq.gptq_gemm(hs[i % n], xs[i % len(xs)], ys[i % len(ys)], M, st)
-        t1.record(st)
-        torch.cuda.synchronize()
-    return t0.elapsed_time(t1) / 1e3 / steps
+        dt = t0.elapsed_time(t1) / 1e3
+        times.append(dt / steps)
+        total += dt
+    del g
+    return statistics.median(times)
+
+
+def layer_line(spec, M, t, hbm, tf_burst, tf_sus):
+    """One (layer, M) result: time, GB/s, TFLOP/s and the roofline fraction (burst and sustained
+    bf16 peaks for tensor-bound cases)."""
+    B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
+    roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
+    r = {"us": round(t * 1e6, 2), "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),
+         "roofline_frac": round(roof / t, 4),
+         "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
+    if r["bound"] == "tensor":
+        r["roofline_frac_sustained"] = round(max(B / (hbm * 1e9), F / (tf_sus * 1e12)) / t, 4)
+    return r
 
 
 def run_native(args, ws, rank, local):
@@ -282,10 +315,12 @@ def run_native(args, ws, rank, local):
     hbm, tf_burst, tf_sus, peak_kind = peaks()
     spec, _ = synth.workload(WORKLOAD)
     M = 1
+    dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
     hs, _ = make_layers(spec, LAYERS)
     xs = [synth.make_x(M, spec.K, spec.dtype, seed=100 + i).cuda() for i in range(LAYERS)]
-    ys = [torch.empty(M, spec.N, dtype=torch.bfloat16, device="cuda") for _ in range(LAYERS)]
+    ys = [torch.empty(M, spec.N, dtype=dt, device="cuda") for _ in range(LAYERS)]
     launches_per_call = gptq.gptq_gemm_launches(hs[0], M)
+    plan = gptq.gptq_gemm_plan(hs[0], M)
 
     def measure():
         barrier(ws)
@@ -296,11 +331,10 @@ def run_native(args, ws, rank, local):
         barrier(ws)
         return max_over_ranks(ws, total), max_over_ranks(ws, eager)
 
-    with ClockSampler(local) as clk:
-        total, eager = measure()
-        # end to end through the public API with host buffers
+    def measure_e2e():
+        # end to end through the public API with host buffers: pinned x in, gptq_gemm, y out
         xh = [synth.make_x(M, spec.K, spec.dtype, seed=100 + i).pin_memory() for i in range(LAYERS)]
-        yh = [torch.empty(M, spec.N, dtype=torch.bfloat16).pin_memory() for _ in range(LAYERS)]
+        yh = [torch.empty(M, spec.N, dtype=dt).pin_memory() for _ in range(LAYERS)]
         st = torch.cuda.current_stream()
         for i in range(args.warmup):
             xs[i % LAYERS].copy_(xh[i % LAYERS], non_blocking=True)
@@ -309,47 +343,69 @@ def run_native(args, ws, rank, local):
         torch.cuda.synchronize()
         barrier(ws)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for i in range(args.steps):
-            xs[i % LAYERS].copy_(xh[i % LAYERS], non_blocking=True)
-            gptq.gptq_gemm(hs[i % LAYERS], xs[i % LAYERS], ys[i % LAYERS], M, st)
-            yh[i % LAYERS].copy_(ys[i % LAYERS], non_blocking=True)
-        e1.record(st)
-        torch.cuda.synchronize()
-        e2e_t = max_over_ranks(ws, e0.elapsed_time(e1) / 1e3 / args.steps)
+        times, tot = [], 0.0
+        while tot < MIN_TIMED_S or len(times) < 5:
+            e0.record(st)
+            for i in range(args.steps):
+                xs[i % LAYERS].copy_(xh[i % LAYERS], non_blocking=True)
+                gptq.gptq_gemm(hs[i % LAYERS], xs[i % LAYERS], ys[i % LAYERS], M, st)
+                yh[i % LAYERS].copy_(ys[i % LAYERS], non_blocking=True)
+            e1.record(st)
+            torch.cuda.synchronize()
+            d = e0.elapsed_time(e1) / 1e3
+            times.append(d / args.steps)
+            tot += d
+        return max_over_ranks(ws, statistics.median(times))
+
+    with ClockSampler(local) as clk:
+        total, eager = measure()
+        e2e_t = measure_e2e()
         barrier(ws)
         extra = {} if (args.no_extra or rank != 0) else extra_workloads(args, hbm, tf_burst, peak_kind, tf_sus)
     clocks = clk.summary()
     bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"} & set(clocks["reasons"])
     if bad and not args._remeasured:
         args._remeasured = True
-        total, eager = measure()
+        with ClockSampler(local) as clk:
+            total, eager = measure()
+        clocks = clk.summary()
 
     B = b_alg(spec, M)
     value = B * ws / total / 1e9
     achieved = B / total / 1e9
-    traffic = traffic_record("gemm_small.cu")
+    traffic = traffic_record("gemm_small.cu", WORKLOAD)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total * 1e3, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
         "us_per_call": round(total * 1e6, 3),
+    }
+    # the other two headline configurations, small and at the top of the line
+    for key in ("decode_m1", "prefill_m4096"):
+        if key in extra:
+            line[key] = extra.pop(key)
+    line.update({
         "config": {"workload": WORKLOAD, "M": M, "K": spec.K, "N": spec.N, "bits": spec.bits,
-                   "group_size": spec.group_size, "zero": "symmetric 8", "act_dtype": "bf16",
-                   "layers_rotated": LAYERS, "l2": f"inputs larger than L2: {LAYERS} resident weight sets "
-                   f"({LAYERS * B / 1e6:.0f} MB) rotated per step", "parallelism": f"replicas x{ws}",
-                   "bytes_per_call": B},
+                   "group_size": spec.group_size, "act_order": spec.desc_act, "zero": "asymmetric",
+                   "act_dtype": spec.dtype, "layers_rotated": LAYERS,
+                   "l2": f"inputs larger than L2: {LAYERS} resident weight sets ({LAYERS * B / 1e6:.0f} MB) "
+                         f"rotated per step", "parallelism": f"replicas x{ws}", "bytes_per_call": B,
+                   "kernel_plan": {"path": "small-M" if plan.path == gptq.PATH_SMALL_M else "large-M",
+                                   "launches": plan.launches, "grid": plan.grid,
+                                   "consumer_warps": plan.consumer_warps,
+                                   "act_order_in_kernel": plan.act_order_in_kernel, "stages": plan.stages}},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
                      "kernel": "k_gemm_small (small-M: persistent TMA-fed weight stream, mma.sync swap-AB)",
-                     "timing": "CUDA events around one replay of a graph of the timed calls"},
+                     "timing": "CUDA events around each replay of a graph of the timed calls; median over "
+                               f"replays totalling >= {MIN_TIMED_S * 1e3:.0f} ms"},
         "eager_us_per_call": round(eager * 1e6, 3),
         "e2e": {"value": round(B * ws / e2e_t / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": 2 * M * spec.K,
                 "d2h_bytes_per_step": 2 * M * spec.N, "us_per_step": round(e2e_t * 1e6, 3)},
         "gpu_launches": launches_per_call * args.steps,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
-    }
+    })
     if rank == 0 and not args.no_cpu_baseline:
         gbs, calls, secs, cores, sample = oracle_sample_rate(spec, M, args.cpu_seconds, 2048)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -394,44 +450,41 @@ def repack_times():
 
 
 def extra_workloads(args, hbm, tf_burst, peak_kind, tf_sus):
-    """Rank 0: the other M values of the decode layer, the 70B gate layer, and prefill."""
+    """Rank 0: the decode layer (M = 1 as a headline key, then 8 and 16), the gate layer's other M,
+    the prefill layer (M = 4096 as a headline key, then 512 and 2048), AWQ and FP8 layers, the
+    K = N = 4096 format sweep, and the load-time repack."""
     import torch
     from weight_only_quantized_gb300 import gptq, synth
     out = {}
     steps = max(20, min(args.steps, 200))
 
-    def one(name, spec, Ms, layers):
+    def one(spec, Ms, layers):
         hs, _ = make_layers(spec, layers, seed0=1000)
-        Mmax = max(Ms)
         for h in hs:
-            gptq.gptq_reserve(h, Mmax)
+            gptq.gptq_reserve(h, max(Ms))
+        dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
         res = {}
         for M in Ms:
             xs = [synth.make_x(M, spec.K, spec.dtype, seed=M + i).cuda() for i in range(min(layers, 4))]
-            dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
             ys = [torch.empty(M, spec.N, dtype=dt, device="cuda") for _ in range(min(layers, 4))]
             n = steps if M <= 64 else max(5, steps // 10)
-            launch = time_calls(hs, xs, ys, M, n, 3, graph=True)
-            B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
-            roof = max(B / (hbm * 1e9), F / (tf_burst * 1e12))
-            res[f"M={M}"] = {"us": round(launch * 1e6, 2), "GB/s": round(B / launch / 1e9, 1),
-                             "TFLOP/s": round(F / launch / 1e12, 2), "roofline_frac": round(roof / launch, 4),
-                             "bound": "hbm" if B / (hbm * 1e9) >= F / (tf_burst * 1e12) else "tensor"}
-            if res[f"M={M}"]["bound"] == "tensor":
-                # against the sustained (power-capped) bf16 rate as well as the burst one
-                res[f"M={M}"]["roofline_frac_sustained"] = round(max(B / (hbm * 1e9), F / (tf_sus * 1e12)) / launch, 4)
+            res[f"M={M}"] = layer_line(spec, M, time_calls(hs, xs, ys, M, n, 3, graph=True), hbm, tf_burst, tf_sus)
             del xs, ys
         for h in hs:
             h.close()
         torch.cuda.empty_cache()
-        out[name] = res
+        return res
 
-    s2, _ = synth.workload(WORKLOAD)
-    one(WORKLOAD, s2, [8, 16], LAYERS)
-    s3, m3 = synth.workload("llama3-70b-gate-8192x28672-b4g128-descact")
-    one("llama3-70b-gate-8192x28672-b4g128-descact", s3, m3, 4)
-    s4, m4 = synth.workload("prefill-8192x28672-b4g128")
-    one("prefill-8192x28672-b4g128", s4, [4096] if args.quick_prefill else m4, 1)
+    s2, _ = synth.workload(DECODE)
+    r2 = one(s2, [1, 8, 16], 16)
+    out["decode_m1"] = dict(r2.pop("M=1"), workload=DECODE)
+    out[DECODE] = r2
+    s3, m3 = synth.workload(WORKLOAD)
+    out[WORKLOAD] = one(s3, [m for m in m3 if m != 1], 8)
+    s4, m4 = synth.workload(PREFILL)
+    r4 = one(s4, [4096] if args.quick_prefill else [4096] + [m for m in m4 if m != 4096], 1)
+    out["prefill_m4096"] = dict(r4.pop("M=4096"), workload=PREFILL)
+    out[PREFILL] = r4
     out["awq-4096x14336-b4g128-fp16"] = awq_layer(hbm, tf_burst)
     out["fp8-4096x14336-block128-bf16"] = fp8_layer(hbm, tf_burst)
     if not args.no_sweep:
@@ -542,8 +595,7 @@ def format_sweep(hbm, tf_burst):
     return res
 
 
-PROFILE_LAYERS = {"decode": WORKLOAD, "gate": "llama3-70b-gate-8192x28672-b4g128-descact",
-                  "prefill": "prefill-8192x28672-b4g128"}
+PROFILE_LAYERS = {"decode": DECODE, "gate": WORKLOAD, "prefill": PREFILL}
 
 
 def run_profile(args):
@@ -558,7 +610,7 @@ def run_profile(args):
     dt = torch.float16 if spec.dtype == "fp16" else torch.bfloat16
     xs = [synth.make_x(M, spec.K, spec.dtype, seed=3).cuda()]
     ys = [torch.empty(M, spec.N, dtype=dt, device="cuda")]
-    t = time_calls(hs, xs, ys, M, args.steps, args.warmup, graph=False)
+    t = time_calls(hs, xs, ys, M, args.steps, args.warmup, graph=False, min_total_s=0.0, min_reps=1)
     B, F = b_alg(spec, M), 2.0 * M * spec.N * spec.K
     print(json.dumps({"profile_layer": args.profile_layer, "M": M, "us_per_call": round(t * 1e6, 2),
                       "GB/s": round(B / t / 1e9, 1), "TFLOP/s": round(F / t / 1e12, 2),

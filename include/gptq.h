@@ -56,6 +56,11 @@ typedef enum {
 
 typedef enum { GPTQ_FP16 = 0, GPTQ_BF16 = 1 } gptq_dtype_t;
 
+/* Size limits of every entry point that builds a handle (UNSUPPORTED beyond them). */
+#define GPTQ_MAX_K      131072   /* in_features  */
+#define GPTQ_MAX_N      262144   /* out_features */
+#define GPTQ_MAX_GROUPS 65536    /* G            */
+
 /* Which kernel family gptq_gemm_path runs.  AUTO is what gptq_gemm does. */
 typedef enum { GPTQ_PATH_AUTO = 0, GPTQ_PATH_SMALL_M = 1, GPTQ_PATH_LARGE_M = 2 } gptq_path_t;
 
@@ -92,7 +97,8 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
  *   g_idx    device, int32 [K], or NULL for the sequential k / group_size.  4-byte aligned.
  *            Any values in [0, G) are accepted; each group's run in sorted order is padded to a
  *            multiple of 32 rows internally, so uneven groups cost bandwidth but stay exact.
- *   K, N     in_features and out_features: K % 32 == 0, N % 32 == 0, 32 <= K, N <= 1<<20.
+ *   K, N     in_features and out_features: K % 32 == 0, N % 32 == 0, 32 <= K <= 131072 and
+ *            32 <= N <= 262144 (GPTQ_MAX_K, GPTQ_MAX_N; UNSUPPORTED above them).
  *   bits     2, 3, 4 or 8.   group_size: -1 (one group) or >= 1; G = ceil(K/group_size).
  *   dtype    dtype of scales, and of x and y in every later gptq_gemm on this handle.
  *   stream   the copy/repack kernels run on it; the call synchronizes it once, at the end, to
@@ -110,6 +116,11 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
 
 /*
  * Make gptq_gemm calls with M <= max_M possible without any allocation inside gptq_gemm.
+ * This is the caller-owned scratch contract of GPTQModel "Kernel Backends Reference", section
+ * "Marlin and caller-owned scratch" (the scratch API and its property table): the workspace
+ * (reduction partials, permuted activations, a zeroed counter array) is sized by a query-free
+ * reserve made before any graph capture, is owned by one stream at a time, and a call never falls
+ * back to allocating when it is too small -- it fails (WORKSPACE) instead.
  * Only a handle whose g_idx order is not the identity (act-order, or groups whose sizes are
  * not multiples of 32) needs workspace above M = 32: max_M * K_sorted activation elements for
  * the permuted copy of x that the kernels read.  It also sizes the large-M kernel's K-split
@@ -198,16 +209,26 @@ gptq_status_t gptq_repack_awq(const int32_t* qweight, const int32_t* qzeros, con
                               gptq_handle_t* out);
 
 /*
- * y = x . W^T for the handle's layer, enqueued on `stream`.
+ * y = x . W^T for the handle's layer, enqueued on `stream` (the spec GEMM of the weight-only
+ * path: weights stream packed from HBM and are dequantised in registers, mlinterviewnotes "Formats
+ * and kernels: FP8, INT8, INT4, Marlin, Machete", opening section and "Where the batch-size
+ * crossover is"; the kernel family is chosen by M, as that page's M-bucketed dispatch describes).
  *   x   device, dtype [M, K] row-major (row stride K elements), 16-byte aligned.
  *   y   device, dtype [M, N] row-major (row stride N elements), 16-byte aligned; x and y must
  *       not overlap.
- *   M   >= 0.  M == 0 returns GPTQ_OK and launches nothing.
+ *   M   >= 0.  M == 0 returns GPTQ_OK and launches nothing: an empty batch is a normal
+ *       steady-state input (a data-parallel rank with no tokens still runs its layers), as the
+ *       same page's discussion of SGLang's M-bucketing after the Machete section points out.
  * Never allocates and never synchronizes.  One handle may be used by one stream at a time
- * (calls on two streams must not overlap on the device: they share the handle's workspace).
+ * (calls on two streams must not overlap on the device: they share the handle's workspace,
+ * GPTQModel "Kernel Backends Reference", scratch ownership: one device, host thread and stream).
  * After gptq_reserve(h, M) has returned, a call with that M may be captured in a CUDA graph.
+ * Timeouts: if an earlier call on this handle gave up a bounded device-side wait (its output was
+ * invalid), the kernel has recorded it in host-visible memory and this call returns
+ * GPTQ_ERR_TIMEOUT without launching anything, until gptq_device_status clears the record.  The
+ * record is read without synchronizing, so it shows the timeouts of kernels that have finished.
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE (M above the reserved size on a path that needs
- * workspace), CUDA.
+ * workspace), TIMEOUT, CUDA.
  */
 gptq_status_t gptq_gemm(gptq_handle_t h, const void* x, void* y, int M, void* stream);
 
@@ -226,7 +247,10 @@ int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
 int gptq_gemm_k_splits(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Free the handle and everything it owns.  Waits for the device to finish using it
- * (cudaDeviceSynchronize on the handle's device).  NULL is accepted. */
+ * (cudaDeviceSynchronize on the handle's device).  NULL is accepted.  A handle is tied to the
+ * buffers it was built from only through its own copy, so rebuilding after any change to the
+ * weights means destroy + repack (GPTQModel "Kernel Backends Reference": do not reuse an initialised
+ * native handle after replacing its buffers; invalidate handles on mutation, checklist item 5). */
 gptq_status_t gptq_destroy(gptq_handle_t h);
 
 /* Sizes of a handle's runtime layout. */
@@ -259,7 +283,9 @@ gptq_status_t gptq_copy_runtime(gptq_handle_t h, void* wr, int32_t* perm, int32_
 /* GPTQ_ERR_TIMEOUT if a kernel launched with this handle gave up a bounded device-side wait (an
  * mbarrier wait that exceeded its time limit; the kernel then skipped its remaining work and the
  * outputs of that call are invalid) since the previous call of this function, else GPTQ_OK.  Clears
- * the record.  Synchronizes the handle's device.  Errors: INVALID_ARG, CUDA. */
+ * the record.  The record lives in mapped (host-visible) memory that the kernels write; this call
+ * reads it without synchronizing anything, so synchronize the stream of the calls in question
+ * first to include them.  Errors: INVALID_ARG. */
 gptq_status_t gptq_device_status(gptq_handle_t h);
 
 /*
@@ -278,9 +304,13 @@ gptq_status_t gptq_device_status(gptq_handle_t h);
  * checkpoint.  kr_capacity = roundup(K + 31*G, 128) and wr_capacity = kr_capacity/128*bits*
  * N_padded*16 always suffice.  Its scratch is a fixed array of 3*4096+8 int32 in device memory
  * that every GPU holds once the library is loaded, so a layer may have at most 4096 groups
- * (GPTQ_ERR_UNSUPPORTED above that).  The first call on a device looks up that array's device
- * address.  Every call on a device shares the array, so calls that overlap on the same GPU race;
- * the call synchronizes `stream` once to read the g_idx histogram.
+ * (GPTQ_ERR_UNSUPPORTED above that).  Every call looks up that array's device address on the
+ * current device (cudaGetSymbolAddress, which allocates nothing).  Every call on a device shares
+ * the array, and the array stays in use until the call's work on `stream` has completed: the call
+ * synchronizes `stream` once, to read the g_idx histogram, but the sort and pack kernels it
+ * enqueues after that still read the array.  So a later call on another stream must first wait
+ * for this call's stream (a stream synchronize or an event); calls that overlap on the GPU race.
+ * Limits on K and N as gptq_repack (GPTQ_MAX_K, GPTQ_MAX_N).
  * Errors: INVALID_ARG, UNSUPPORTED, SHAPE, ALIGNMENT, DEVICE, INVALID_GIDX, WORKSPACE (output
  * buffers too small for the sorted K), CUDA.
  */
@@ -290,7 +320,38 @@ gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32_t* qzeros,
                                   int32_t* cgid, int kr_capacity, void* s_r, uint8_t* z_r,
                                   int* k_sorted, void* stream);
 
-/* Static text for a status. */
+/* The launch plan gptq_gemm_path would use at this M (host only, no device work), for checking
+ * which kernel variant a test or a benchmark actually exercises. */
+typedef struct {
+  int path;            /* GPTQ_PATH_SMALL_M or GPTQ_PATH_LARGE_M                               */
+  int launches;        /* kernels per call (an activation gather or permute counts as one)     */
+  int grid;            /* CTAs of the GEMM kernel                                               */
+  int threads;         /* threads per CTA                                                       */
+  int smem_bytes;      /* dynamic shared memory per CTA                                         */
+  int consumer_warps;  /* small-M: warps that dequantise and multiply; large-M: 4 dequantisers  */
+  int m_tiles;         /* small-M: 8-row m-tiles (1, 2, 4); large-M: x rows per tile (64..256)  */
+  int act_order_in_kernel; /* small-M: 1 when x is permuted in shared memory (no pre-pass)      */
+  int k_splits;        /* CTAs that share one output tile's K (1 = no split)                    */
+  int k_panels;        /* small-M: K panels x is staged in (1 = all of K at once)               */
+  int stages;          /* weight ring depth                                                     */
+} gptq_plan_t;
+
+/* Errors: INVALID_ARG (bad handle, M < 1, unknown path, M above the small-M kernel's 32 rows),
+ * UNSUPPORTED (no plan fits this layer). */
+gptq_status_t gptq_gemm_plan(gptq_handle_t h, int M, gptq_path_t path, gptq_plan_t* plan);
+
+/* Test hook for the error path of the bounded waits; not for production use.  While `on` is 1,
+ * the small-M kernel's copy producer issues no copy at all, so nothing is ever in flight and every
+ * consumer wait runs into its limit, which is `wait_limit_ns` (e.g. 1000000 for 1 ms) instead of the
+ * normal 2 s.  The call's output is then invalid and the handle records GPTQ_ERR_TIMEOUT (see
+ * gptq_gemm and gptq_device_status).  on = 0 restores normal operation and the 2 s limit.
+ * Errors: INVALID_ARG. */
+gptq_status_t gptq_set_test_stall(gptq_handle_t h, int on, uint64_t wait_limit_ns);
+
+/* Static text for a status: the name of the code.  Together with gptq_last_error_message, which
+ * names the violated rule, this is the "fail rather than silently fall back" error contract of
+ * GPTQModel "Kernel Backends Reference" (scratch property table: invalid buffers fail) and of
+ * tensref.org "GPTQ packed checkpoint", section "Reject the file when". */
 const char* gptq_status_string(gptq_status_t s);
 
 /* Text of the calling thread's most recent failure ("" if none).  Valid until the next call. */

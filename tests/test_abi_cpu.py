@@ -96,3 +96,63 @@ def test_null_handle_calls():
     assert L.gptq_destroy(None) == 0
     assert L.gptq_gemm_launches(None, 1, 0) == -1
     assert L.gptq_get_info(None, None) == 1
+
+
+def test_null_handle_plan_and_stall_hook():
+    L = gptq.lib()
+    plan = gptq.GptqPlan()
+    assert L.gptq_gemm_plan(None, 1, 0, C.byref(plan)) == 1
+    assert L.gptq_set_test_stall(None, 1, 1000000) == 1
+
+
+def _noalloc_args(K=512, N=256, bits=4, gs=128):
+    import torch
+    from weight_only_quantized_gb300 import synth
+    ck = synth.make_checkpoint(synth.LayerSpec(K, N, bits, gs), seed=3)
+    G, Np = ck.spec.G, -(-N // 256) * 256
+    kr_cap = -(-(K + 31 * G) // 128) * 128
+    bufs = dict(wr=torch.empty(kr_cap // 128 * bits * Np * 16, dtype=torch.uint8),
+                perm=torch.empty(kr_cap, dtype=torch.int32), cgid=torch.empty(kr_cap // 32, dtype=torch.int32),
+                s_r=torch.empty((G, Np), dtype=torch.int16), z_r=torch.empty((G, Np), dtype=torch.uint8))
+    return ck, bufs
+
+
+@pytest.mark.parametrize("short", ["cgid", "s_r", "z_r"])
+def test_noalloc_wrapper_rejects_short_outputs_before_any_launch(short):
+    """The C entry point takes no capacity for cgid, s_r and z_r, so the binding checks them: a short
+    one is refused on the host, before the library is called (these CPU tensors would be refused as
+    not on the GPU only after the sizes)."""
+    import torch
+    ck, b = _noalloc_args()
+    b[short] = b[short].flatten()[:-1] if short != "cgid" else b[short][:-1]
+    with pytest.raises(gptq.GptqError) as ei:
+        gptq.gptq_repack_noalloc(ck.qweight, ck.qzeros, ck.scales, None, 4, 128, b["wr"], b["perm"], b["cgid"],
+                                 b["s_r"], b["z_r"])
+    assert ei.value.status == 1 and short in str(ei.value)
+
+
+def test_noalloc_wrapper_rejects_wrong_dtype_and_host_tensors():
+    import torch
+    ck, b = _noalloc_args()
+    bad = dict(b, perm=b["perm"].view(torch.float32))
+    with pytest.raises(gptq.GptqError) as ei:
+        gptq.gptq_repack_noalloc(ck.qweight, ck.qzeros, ck.scales, None, 4, 128, **bad)
+    assert ei.value.status == 1 and "int32" in str(ei.value)
+    with pytest.raises(gptq.GptqError) as ei:     # right sizes, but host memory
+        gptq.gptq_repack_noalloc(ck.qweight, ck.qzeros, ck.scales, None, 4, 128, **b)
+    assert ei.value.status == 1 and "CUDA device" in str(ei.value)
+
+
+def test_limits_shared_by_header_and_library():
+    text = open(HEADER).read()
+    assert "#define GPTQ_MAX_K      131072" in text and "#define GPTQ_MAX_N      262144" in text
+    L = gptq.lib()
+    out = C.c_void_p()
+    dummy = C.c_void_p(4096)
+    # one step past each limit is refused before any device work, by both repack entry points
+    assert L.gptq_repack(dummy, dummy, dummy, None, 131072 + 32, 256, 4, 128, 0, None, C.byref(out)) == 2
+    assert L.gptq_repack(dummy, dummy, dummy, None, 256, 262144 + 32, 4, 128, 0, None, C.byref(out)) == 2
+    kr = C.c_int()
+    args = [dummy, dummy, dummy, None, 131072 + 32, 256, 4, 128, 0, dummy, C.c_size_t(1 << 40), dummy, dummy,
+            1 << 20, dummy, dummy, C.byref(kr), None]
+    assert L.gptq_repack_noalloc(*args) == 2

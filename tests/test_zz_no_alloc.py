@@ -56,16 +56,28 @@ def test_noalloc_repack_matches_gptq_repack_twice():
 
 
 def test_noalloc_rejects_too_many_groups_and_small_buffers():
-    spec = synth.LayerSpec(8192 * 4, 64, 4, 4, False, False, "fp16")     # 8192 groups > 4096
+    # 8192 groups > the fixed scratch's 4096: refused by the library (the outputs are sized right, so
+    # the binding's own checks pass)
+    spec = synth.LayerSpec(8192 * 4, 64, 4, 4, False, False, "fp16")
     ck = synth.make_checkpoint(spec, seed=1)
-    tiny = torch.empty(16, dtype=torch.int32, device="cuda")
+    G, Np = spec.G, 256
+    kr_cap = -(-(spec.K + 31 * G) // 128) * 128
+    perm = torch.empty(kr_cap, dtype=torch.int32, device="cuda")
+    cgid = torch.empty(kr_cap // 32, dtype=torch.int32, device="cuda")
+    s_r = torch.empty((G, Np), dtype=torch.int16, device="cuda")
+    z_r = torch.empty((G, Np), dtype=torch.uint8, device="cuda")
+    wr = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(gptq.GptqError) as ei:
         gptq.gptq_repack_noalloc(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(), None, 4, 4,
-                                 tiny.view(torch.uint8), tiny, tiny, tiny, tiny.view(torch.uint8))
+                                 wr, perm, cgid, s_r, z_r)
     assert ei.value.status == 2 and "4096" in str(ei.value)
+    # code and perm buffers smaller than the sorted K: refused after the histogram, nothing written
     spec = synth.LayerSpec(512, 256, 4, 128)
     ck = synth.make_checkpoint(spec, seed=2)
+    tiny = torch.empty(16, dtype=torch.int32, device="cuda")
+    s_r = torch.empty((spec.G, 256), dtype=torch.int16, device="cuda")
+    z_r = torch.empty((spec.G, 256), dtype=torch.uint8, device="cuda")
     with pytest.raises(gptq.GptqError) as ei:
         gptq.gptq_repack_noalloc(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(), None, 4, 128,
-                                 tiny.view(torch.uint8), tiny, tiny, tiny, tiny.view(torch.uint8))
+                                 tiny.view(torch.uint8), tiny, tiny, s_r, z_r)
     assert ei.value.status == 6

@@ -13,9 +13,9 @@ namespace gptq {
 
 namespace {
 thread_local std::string g_last_error;
-constexpr int kMaxK = 1 << 17;        // in_features limit (index arithmetic and repack cost)
-constexpr int kMaxN = 1 << 18;        // out_features limit
-constexpr int kMaxGroups = 1 << 16;
+constexpr int kMaxK = GPTQ_MAX_K;        // in_features limit (index arithmetic and repack cost)
+constexpr int kMaxN = GPTQ_MAX_N;        // out_features limit
+constexpr int kMaxGroups = GPTQ_MAX_GROUPS;
 // Largest M routed to the small-M (mma.sync weight-streaming) kernel by gptq_gemm.  Up to M = 16
 // the layer is HBM-bound on GB300 (ridge M* = P * 4.125 / (16 * BW) ~ 72 for 4-bit group 128) and
 // the swap-AB mma.sync kernel keeps every SM streaming weights.  With four m-tiles it also beats
@@ -51,7 +51,7 @@ static void free_handle(Handle* h) {
   cudaFree(h->scale_inv);
   cudaFree(h->ws);
   cudaFree(h->ws_cnt);
-  cudaFree(h->err);
+  if (h->err_host) cudaFreeHost(const_cast<int32_t*>(h->err_host));
   delete h;
 }
 
@@ -92,6 +92,9 @@ static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, 
   if (dev != h.device)
     return fail(GPTQ_ERR_INVALID_ARG, "handle belongs to device " + std::to_string(h.device) +
                                           " but device " + std::to_string(dev) + " is current");
+  if (*h.err_host != DEV_ERR_NONE)
+    return fail(GPTQ_ERR_TIMEOUT, "an earlier call on this handle gave up a bounded device-side wait and its output "
+                                  "was invalid; gptq_device_status clears the record");
   if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
   if (path == GPTQ_PATH_LARGE_M && !large_m_available())
     return fail(GPTQ_ERR_UNSUPPORTED, "the large-M kernel is not part of this build");
@@ -160,7 +163,7 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
   if (g_idx_len != 0 && g_idx_len != K)
     return fail(GPTQ_ERR_SHAPE, "GPTQ-004: g_idx length must equal in_features = " + std::to_string(K));
   if (K > kMaxK || N > kMaxN || G > kMaxGroups)
-    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= 131072, N <= 262144, groups <= 65536)");
+    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= " + std::to_string(kMaxK) + ", N <= " + std::to_string(kMaxN) + ", groups <= " + std::to_string(kMaxGroups) + ")");
   if (in_features) *in_features = (int)K;
   if (out_features) *out_features = (int)N;
   return GPTQ_OK;
@@ -189,7 +192,7 @@ static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, con
   if (N < 32 || N % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a positive multiple of 32");
   const int G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
   if (K > kMaxK || N > kMaxN || G > kMaxGroups)
-    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= 131072, N <= 262144, groups <= 65536)");
+    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= " + std::to_string(kMaxK) + ", N <= " + std::to_string(kMaxN) + ", groups <= " + std::to_string(kMaxGroups) + ")");
   if (flags & ~(unsigned)(GPTQ_REPACK_ZEROS_V2 | GPTQ_REPACK_SCALES_FP32))
     return fail(GPTQ_ERR_INVALID_ARG, "unknown repack flag bits");
   const bool sf32 = (flags & GPTQ_REPACK_SCALES_FP32) != 0;
@@ -210,9 +213,13 @@ static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, con
   h->zoff = (fmt != kFmtGptq || (flags & GPTQ_REPACK_ZEROS_V2)) ? 0 : 1;
   h->fp8 = fp8 ? 1 : 0;
   h->kb = (K + 127) / 128;
-  cudaError_t ce = cudaMalloc(&h->err, sizeof(int32_t));
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(h->err, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
-  if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaMalloc(error word)"); }
+  void* eh = nullptr;
+  cudaError_t ce = cudaHostAlloc(&eh, sizeof(int32_t), cudaHostAllocMapped);
+  if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaHostAlloc(error word)"); }
+  h->err_host = static_cast<volatile int32_t*>(eh);
+  *h->err_host = DEV_ERR_NONE;
+  ce = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->err), eh, 0);
+  if (ce != cudaSuccess) { free_handle(h); return cuda_fail(ce, "cudaHostGetDevicePointer(error word)"); }
   s = build_runtime(*h, qweight, qzeros, scales, g_idx, fmt, sf32, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
@@ -388,11 +395,8 @@ gptq_status_t gptq_destroy(gptq_handle_t hh) {
 gptq_status_t gptq_device_status(gptq_handle_t hh) {
   if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
   Handle& h = *reinterpret_cast<Handle*>(hh);
-  int32_t word = 0;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpy(&word, h.err, sizeof(word), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && word != DEV_ERR_NONE) e = cudaMemset(h.err, 0, sizeof(int32_t));
-  if (e != cudaSuccess) return cuda_fail(e, "gptq_device_status");
+  const int32_t word = *h.err_host;
+  if (word != DEV_ERR_NONE) *h.err_host = DEV_ERR_NONE;
   if (word == DEV_ERR_TIMEOUT)
     return fail(GPTQ_ERR_TIMEOUT, "a kernel gave up a bounded wait on an mbarrier; that call's output is invalid");
   return GPTQ_OK;
@@ -431,6 +435,41 @@ gptq_status_t gptq_copy_runtime(gptq_handle_t hh, void* wr, int32_t* perm, int32
     return cuda_fail(e, "copy s_r");
   if (z_r && h.z_r && (e = cudaMemcpy(z_r, h.z_r, (size_t)h.G * h.Np, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "copy z_r");
+  return GPTQ_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+gptq_status_t gptq_gemm_plan(gptq_handle_t hh, int M, gptq_path_t path, gptq_plan_t* plan) {
+  if (!hh || !plan) return fail(GPTQ_ERR_INVALID_ARG, "handle and plan are required");
+  if (M < 1) return fail(GPTQ_ERR_INVALID_ARG, "M must be >= 1");
+  if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M)
+    return fail(GPTQ_ERR_INVALID_ARG, "unknown path");
+  const Handle& h = *reinterpret_cast<const Handle*>(hh);
+  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  std::memset(plan, 0, sizeof(*plan));
+  plan->path = path;
+  if (path == GPTQ_PATH_SMALL_M) {
+    if (M > small_m_max())
+      return fail(GPTQ_ERR_INVALID_ARG, "M = " + std::to_string(M) + " is above the small-M kernel's " +
+                                            std::to_string(small_m_max()) + " rows");
+    if (!small_m_plan_info(h, M, plan)) return fail(GPTQ_ERR_UNSUPPORTED, "no small-M plan fits this layer");
+  } else if (!large_m_plan_info(h, M, plan)) {
+    return fail(GPTQ_ERR_UNSUPPORTED, "no large-M plan fits this layer");
+  }
+  return GPTQ_OK;
+}
+
+gptq_status_t gptq_set_test_stall(gptq_handle_t hh, int on, uint64_t wait_limit_ns) {
+  if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
+  if (on != 0 && on != 1) return fail(GPTQ_ERR_INVALID_ARG, "on must be 0 or 1");
+  if (on && (wait_limit_ns < 1000 || wait_limit_ns > 2000000000ull))
+    return fail(GPTQ_ERR_INVALID_ARG, "wait_limit_ns must lie in [1 us, 2 s]");
+  Handle& h = *reinterpret_cast<Handle*>(hh);
+  h.test_stall = on;
+  h.wait_ns = on ? wait_limit_ns : 2000000000ull;
   return GPTQ_OK;
 }
 

@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         }
       }
     }
-    if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+    if (!ok) report_timeout(a.err);
     uint16_t* y = static_cast<uint16_t*>(a.y);
     if (a.split > 1) {
       // this K range's partial, then the tile's counter (every CTA counts once, also after a timeout,
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         // every issued copy must land before the CTA may exit
         for (int i = x_issued > XS ? x_issued - XS : 0; i < x_issued; ++i)
           if (!mbar_wait(x_full(i % XS), (i / XS) & 1)) ok = false;
-        if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+        if (!ok) report_timeout(a.err);
       }
     } else if (warp == 2) {
       // ---------------- packed-code producer: codes and stored zeros of each block ----------------
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         }
         for (int b = pk_issued > PS ? pk_issued - PS : 0; b < pk_issued; ++b)
           if (!mbar_wait(pk_full(b % PS), (b / PS) & 1)) ok = false;
-        if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+        if (!ok) report_timeout(a.err);
       }
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
@@ -579,9 +579,12 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
           if (++ws == WS) { ws = 0; wph ^= 1u; }
         }
         // every MMA must have landed before tensor memory is released
+        // (after a timeout the issued MMAs still complete -- they only read shared memory -- so the
+        // drain takes a fresh limit: tensor memory must never be freed under an MMA in flight)
         umma_commit_if(mma_done, me);
-        mbar_wait_poison(mma_done, 0, limit);
-        if (limit == 0 && me) atomicExch(a.err, DEV_ERR_TIMEOUT);
+        uint64_t drain = kWaitLimitNs;
+        mbar_wait_poison(mma_done, 0, drain);
+        if ((limit == 0 || drain == 0) && me) report_timeout(a.err);
       }
     } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDq) {
       // ---------------- dequantisers: thread owns weight row n0 + nrow ----------------
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
         __syncwarp();
         if (lane == 0) mbar_arrive(pk_empty(ps));           // both halves of this block are written
       }
-      if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+      if (!ok) report_timeout(a.err);
     }
   }
 
@@ -787,6 +790,24 @@ EncodeTiledFn encode_fn() {
 bool large_m_available() { return true; }
 
 int large_m_launches(const Handle& h, int M) { return M > 0 ? (h.identity ? 1 : 2) : 0; }
+
+bool large_m_plan_info(const Handle& h, int M, gptq_plan_t* out) {
+  const int bmx = M > 0 ? large_bmx(h, M) : 0;
+  if (bmx == 0) return false;
+  const int split = large_split(h, M);
+  out->path = GPTQ_PATH_LARGE_M;
+  out->launches = large_m_launches(h, M);
+  out->grid = (M + bmx - 1) / bmx * (h.Np / BN) * split;
+  out->threads = kThreadsL;
+  out->smem_bytes = (int)smem_bits(h.fp8 ? 8 : h.bits, bmx, h.Kr);
+  out->consumer_warps = kDqWarps;
+  out->m_tiles = bmx;
+  out->act_order_in_kernel = 0;
+  out->k_splits = split;
+  out->k_panels = 1;
+  out->stages = bmx == 256 ? 3 : 4;
+  return true;
+}
 
 cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
   const int bmx = large_bmx(h, M);

@@ -271,6 +271,8 @@ struct SmallArgs {
                     // start is not hidden behind the previous call); 0: every thread loads it at start
   int zoff;         // zero = stored byte + zoff (1: GPTQ v1 fields, stored minus one; 0: gptq_v2, AWQ)
   const float* bias;   // [Np] float32 added to y, or nullptr
+  uint64_t wait_ns; // limit of every bounded wait
+  int stall;        // test hook: the producer issues no copy, so every wait runs into its limit
 };
 
 template <int CW>
@@ -341,8 +343,9 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     // copies branches on a shared-memory value: the waits only poison the limit (an early-exit
     // branch on a wait result made each issue wait for the previous copy, ~4x slower here).
     uint32_t go = elect_one();
+    if (a.stall) go = 0u;
     const uint64_t stream_policy = l2_evict_first();
-    uint64_t limit = kWaitNs;
+    uint64_t limit = a.wait_ns;
     bool waited = false;            // griddepcontrol.wait done (x may be the previous grid's output)
     int s_issued = 0;               // weight stages issued
     int q = 0;                      // segments (tile, panel) started
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int qq = q_sent > 2 ? q_sent - 2 : 0; qq < q_sent; ++qq)
       mbar_wait_poison(hfull(qq & 1), (uint32_t)((qq >> 1) & 1), drain);
     if (cg_sent) mbar_wait_poison(cgfull, 0u, drain);
-    if ((limit == 0 || drain == 0) && lane == 0) atomicExch(a.err, DEV_ERR_TIMEOUT);
+    if ((limit == 0 || drain == 0) && lane == 0) report_timeout(a.err);
     return;
   }
 
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 #pragma unroll
         for (int r = 0; r < 4; ++r) xsp[mt][r] = 0.f;
   };
-  if (a.cg_async && !mbar_wait(cgfull, 0u)) ok = false;   // the chunk-group table (no block runs without it)
+  if (a.cg_async && !mbar_wait(cgfull, 0u, a.wait_ns)) ok = false;   // the chunk-group table (no block runs without it)
   int s_base = 0;
   int q = 0;
   for (int ti = T0; ti < T1; ++ti) {
@@ -492,17 +495,20 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int p = 0; p < a.npanel; ++p, ++q) {
       const int nb = panel_blocks(p);
       const int hs = q & 1;
-      if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1))) ok = false;
+      if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1), a.wait_ns)) ok = false;
       if (GATHER && q == 0) {
-        // x[m][perm[j]] from the copied rows into the staged rows, two sorted rows per store
-        const int half = a.Kr / 2;
-        const uint16_t* rx = reinterpret_cast<const uint16_t*>(rawx);
-        for (int i = tid; i < half; i += kCW * 32) {
-          const int k0 = pm[2 * i], k1 = pm[2 * i + 1];
-          for (int m = 0; m < a.M; ++m) {
-            const uint32_t lo = k0 >= 0 ? rx[(size_t)m * a.ldx + k0] : 0u;
-            const uint32_t hi = k1 >= 0 ? rx[(size_t)m * a.ldx + k1] : 0u;
-            *reinterpret_cast<uint32_t*>(xreg + m * a.x_row + 4 * i) = lo | (hi << 16);
+        // x[m][perm[j]] from the copied rows into the staged rows, two sorted rows per store (only
+        // after the copy of perm has landed: after a timeout the indices would be garbage)
+        if (ok) {
+          const int half = a.Kr / 2;
+          const uint16_t* rx = reinterpret_cast<const uint16_t*>(rawx);
+          for (int i = tid; i < half; i += kCW * 32) {
+            const int k0 = pm[2 * i], k1 = pm[2 * i + 1];
+            for (int m = 0; m < a.M; ++m) {
+              const uint32_t lo = k0 >= 0 ? rx[(size_t)m * a.ldx + k0] : 0u;
+              const uint32_t hi = k1 >= 0 ? rx[(size_t)m * a.ldx + k1] : 0u;
+              *reinterpret_cast<uint32_t*>(xreg + m * a.x_row + 4 * i) = lo | (hi << 16);
+            }
           }
         }
         named_sync_consumers<kCW>();      // every consumer's share of x is in place
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
             zw0 = *reinterpret_cast<const uint32_t*>(zrow + 4 * g);
             sw0 = *reinterpret_cast<const uint2*>(zrow + 32 + 8 * g);
           }
-          if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1))) { ok = false; break; }
+          if (!mbar_wait(full(slot), (uint32_t)((s >> lg) & 1), a.wait_ns)) { ok = false; break; }
           if (lb >= nb) {
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(slot));
@@ -717,7 +723,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       }
     }
   }
-  if (!ok) atomicExch(a.err, DEV_ERR_TIMEOUT);
+  if (!ok) report_timeout(a.err);
 }
 
 // xp[m][j] = x[m][perm[j]] (0 for pad rows): activations in sorted k order for the bulk copies.
@@ -874,7 +880,7 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
-                 h.zoff, h.has_bias ? h.bias : nullptr};
+                 h.zoff, h.has_bias ? h.bias : nullptr, h.wait_ns, h.test_stall};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
@@ -917,6 +923,23 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 }  // namespace
 
 int small_m_max() { return 32; }
+
+bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out) {
+  SmallPlan p{};
+  if (M < 1 || M > 32 || !make_plan(h, M, p)) return false;
+  out->path = GPTQ_PATH_SMALL_M;
+  out->launches = (h.identity || p.gather) ? 1 : 2;
+  out->grid = p.grid;
+  out->threads = p.cw == 16 ? threads_of<16>() : threads_of<8>();
+  out->smem_bytes = p.smem;
+  out->consumer_warps = p.cw;
+  out->m_tiles = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  out->act_order_in_kernel = p.gather;
+  out->k_splits = 1;
+  out->k_panels = p.npanel;
+  out->stages = 1 << p.lg_rd;
+  return true;
+}
 
 int small_m_launches(const Handle& h, int M) {
   if (M <= 0) return 0;

@@ -50,7 +50,15 @@ struct Handle {
   std::vector<int32_t> cgid_host;   // host copy of cgid (split planning)
   CUtensorMap wr_map;               // wr as uint64 [Kr/128 * bits rows][2 Np]: one box = kSmallBlocksPerBox
                                     // blocks of one 32-column tile (small-M path)
-  int32_t* err = nullptr;    // device error word: kernels set it when a bounded wait gives up
+  // Error word in mapped, pinned host memory: the kernels store DEV_ERR_TIMEOUT into it when a
+  // bounded wait gives up, and the host reads it without synchronizing (err is the device view of
+  // err_host).
+  int32_t* err = nullptr;
+  volatile int32_t* err_host = nullptr;
+  // Limit of every bounded wait of the small-M kernel, and the test hook that makes its producer
+  // issue nothing (gptq_set_test_stall).
+  uint64_t wait_ns = 2000000000ull;
+  int test_stall = 0;
   // workspace
   int reserved_M = 0;
   void* xp = nullptr;        // [reserved_M][Kr] activations in sorted order (large-M path)
@@ -122,11 +130,13 @@ int large_tile_count(const Handle& h, int M);   // output tiles (x tile x 128 we
 int small_m_launches(const Handle& h, int M);
 int small_m_max();   // largest M the small-M kernel covers (four m-tiles of 8 rows)
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
+bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out);   // false: no plan fits
 
 // Large-M path: tcgen05 / TMEM / TMA kernel (plus an x-permute pre-pass when not identity).
 bool large_m_available();
 int large_m_launches(const Handle& h, int M);
 cudaError_t launch_gemm_large(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
+bool large_m_plan_info(const Handle& h, int M, gptq_plan_t* out);   // false: no plan fits
 
 // ---- device helpers ----
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
@@ -152,6 +162,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 // Device error codes written to Handle::err (0 = none).
 enum : int32_t { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1 };
+// Record a timeout in the handle's error word, which lives in mapped host memory: a plain
+// system-visible store (every writer stores the same value), then a fence so the host sees it.
+__device__ __forceinline__ void report_timeout(int32_t* err) {
+  *reinterpret_cast<volatile int32_t*>(err) = DEV_ERR_TIMEOUT;
+  __threadfence_system();
+}
 
 // ---- mbarrier and bulk-copy helpers (sm_90+ PTX) ----
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

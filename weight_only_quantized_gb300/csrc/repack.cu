@@ -379,32 +379,14 @@ gptq_status_t build_runtime(Handle& h, const void* qweight, const int32_t* qzero
 // Allocation-free repack (gptq_repack_noalloc).  Its only scratch, the per-group counts, offsets
 // and cursors of the sort plus a few flags, lives in this file-scope device array, which every
 // device that loads the library holds until the process exits.  In host code the array's name is
-// a host-side stand-in, so its device address is looked up once per device with
-// cudaGetSymbolAddress (on the first call made with that device current) and passed to the
-// kernels.  All calls on a device share the array: the counts are cleared by k_histogram and the
-// cursors by a memset on every call, and calls that overlap on the same GPU (for example on two
-// streams) race on it.
+// a host-side stand-in, so every call looks up its device address on the current device with
+// cudaGetSymbolAddress (cheap next to the stream synchronize the call makes anyway, and never stale
+// after the context is torn down and created again) and passes that address to the kernels.  All
+// calls on a device share the array: the counts are cleared by k_histogram and the cursors by a
+// memset on every call, and the array is in use until the call's kernels on its stream have
+// finished, so calls that overlap on the same GPU (for example on two streams) race on it.
 constexpr int kNoallocMaxGroups = 4096;
 static __device__ __align__(256) int32_t g_noalloc_scratch[3 * kNoallocMaxGroups + M_N];
-
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on the first call there).
-cudaError_t noalloc_scratch(int dev, int32_t** out) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
-  return cudaSuccess;
-}
-}  // namespace
 
 }  // namespace gptq
 
@@ -421,8 +403,11 @@ extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32
     return fail(GPTQ_ERR_UNSUPPORTED, "GPTQ-001: bits must be 2, 3, 4 or 8, got " + std::to_string(bits));
   if (dtype != GPTQ_FP16 && dtype != GPTQ_BF16) return fail(GPTQ_ERR_UNSUPPORTED, "dtype must be GPTQ_FP16 or GPTQ_BF16");
   if (group_size != -1 && group_size < 1) return fail(GPTQ_ERR_INVALID_ARG, "group_size must be -1 or >= 1");
-  if (K < 32 || K % 32 != 0 || K > (1 << 17)) return fail(GPTQ_ERR_SHAPE, "GPTQ-002: in_features must be a multiple of 32 in [32, 131072]");
-  if (N < 32 || N % 32 != 0 || N > (1 << 18)) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a multiple of 32 in [32, 262144]");
+  if (K < 32 || K % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-002: in_features must be a positive multiple of 32");
+  if (N < 32 || N % 32 != 0) return fail(GPTQ_ERR_SHAPE, "GPTQ-003: out_features must be a positive multiple of 32");
+  if (K > GPTQ_MAX_K || N > GPTQ_MAX_N)
+    return fail(GPTQ_ERR_UNSUPPORTED, "layer too large for this build (K <= " + std::to_string(GPTQ_MAX_K) +
+                                          ", N <= " + std::to_string(GPTQ_MAX_N) + ")");
   const int G = group_size == -1 ? 1 : (K + group_size - 1) / group_size;
   if (G > kNoallocMaxGroups)
     return fail(GPTQ_ERR_UNSUPPORTED, "gptq_repack_noalloc: at most " + std::to_string(kNoallocMaxGroups) +
@@ -435,14 +420,14 @@ extern "C" gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(GPTQ_ERR_DEVICE, "device ordinal out of range");
   int major = 0, minor = 0;
   if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute");
   if (major != 10 || minor != 3) return fail(GPTQ_ERR_DEVICE, "this library is built for sm_103a (compute capability 10.3)");
   int32_t* scratch = nullptr;
-  if ((e = noalloc_scratch(dev, &scratch)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(repack scratch)");
+  if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&scratch), g_noalloc_scratch)) != cudaSuccess)
+    return cuda_fail(e, "cudaGetSymbolAddress(repack scratch)");
   int32_t* cnt = scratch;
   int32_t* off = scratch + G;
   int32_t* cursor = scratch + 2 * G;

@@ -38,6 +38,13 @@ class GptqInfo(C.Structure):
                 ("device_bytes", C.c_size_t)]
 
 
+class GptqPlan(C.Structure):
+    _fields_ = [("path", C.c_int), ("launches", C.c_int), ("grid", C.c_int), ("threads", C.c_int),
+                ("smem_bytes", C.c_int), ("consumer_warps", C.c_int), ("m_tiles", C.c_int),
+                ("act_order_in_kernel", C.c_int), ("k_splits", C.c_int), ("k_panels", C.c_int),
+                ("stages", C.c_int)]
+
+
 SIGNATURES = {
     "gptq_check_shapes": (_I, [_I, _L, _L, _L, _L, _L, _L, _L, _I, _P, _P]),
     "gptq_repack": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
@@ -55,6 +62,8 @@ SIGNATURES = {
     "gptq_copy_runtime": (_I, [_P, _P, _P, _P, _P, _P]),
     "gptq_device_status": (_I, [_P]),
     "gptq_repack_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, C.c_size_t, _P, _P, _I, _P, _P, _P, _P]),
+    "gptq_gemm_plan": (_I, [_P, _I, _I, C.POINTER(GptqPlan)]),
+    "gptq_set_test_stall": (_I, [_P, _I, C.c_uint64]),
     "gptq_status_string": (C.c_char_p, [_I]),
     "gptq_last_error_message": (C.c_char_p, []),
 }
@@ -266,16 +275,50 @@ def gptq_repack_noalloc(qweight: torch.Tensor, qzeros: torch.Tensor, scales: tor
     """Repack into caller-owned device tensors; the library allocates nothing.  Returns K_sorted.
 
     wr: uint8 (capacity = numel), perm: int32 [kr_capacity], cgid: int32 [kr_capacity // 32],
-    s_r: fp16/bf16-sized 2-byte [G, N_padded], z_r: uint8 [G, N_padded]."""
+    s_r: fp16/bf16-sized 2-byte [G, N_padded], z_r: uint8 [G, N_padded].  Every output is checked
+    (dtype, contiguity, size, device) before the library is called, since the C entry point takes no
+    capacity for cgid, s_r and z_r."""
     K, N = gptq_check_shapes(bits, tuple(qweight.shape), tuple(qzeros.shape), tuple(scales.shape),
                              0 if g_idx is None else g_idx.numel(), group_size)
     if scales.dtype not in DTYPE:
         raise GptqError(2, "scales must be fp16 or bf16")
+    G = 1 if group_size == -1 else -(-K // group_size)
+    Np = -(-N // 256) * 256
+    outs = (("wr", wr, 1), ("perm", perm, 4), ("cgid", cgid, 4), ("s_r", s_r, 2), ("z_r", z_r, 1))
+    for name, t, es in outs:
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous() or t.element_size() != es:
+            raise GptqError(1, f"{name} must be a contiguous tensor of {es}-byte elements")
+    if perm.dtype != torch.int32 or cgid.dtype != torch.int32:
+        raise GptqError(1, "perm and cgid must be int32")
+    if z_r.dtype != torch.uint8:
+        raise GptqError(1, "z_r must be uint8")
+    if cgid.numel() * 32 < perm.numel():
+        raise GptqError(1, f"cgid holds {cgid.numel()} chunks; perm's capacity of {perm.numel()} rows needs "
+                           f"{-(-perm.numel() // 32)}")
+    if s_r.numel() < G * Np or z_r.numel() < G * Np:
+        raise GptqError(1, f"s_r and z_r need at least G * N_padded = {G} * {Np} elements")
+    dev = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t, _ in outs:
+        if not t.is_cuda or t.device.index != dev:
+            raise GptqError(1, f"{name} must be on the current CUDA device")
     kr = C.c_int()
     _check(lib().gptq_repack_noalloc(_ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(g_idx), K, N, bits, group_size,
                                      DTYPE[scales.dtype], _ptr(wr), wr.numel() * wr.element_size(), _ptr(perm),
                                      _ptr(cgid), perm.numel(), _ptr(s_r), _ptr(z_r), C.byref(kr), _stream(stream)))
     return kr.value
+
+
+def gptq_gemm_plan(h: Handle, M: int, path: int = PATH_AUTO) -> GptqPlan:
+    """The launch plan gptq_gemm_path would use at M (host only)."""
+    plan = GptqPlan()
+    _check(lib().gptq_gemm_plan(h.ptr, M, path, C.byref(plan)))
+    return plan
+
+
+def gptq_set_test_stall(h: Handle, on: bool, wait_limit_ns: int = 1_000_000):
+    """Test hook: the small-M kernel's producer issues no copy and every wait gives up after
+    wait_limit_ns (see include/gptq.h).  Not for production use."""
+    _check(lib().gptq_set_test_stall(h.ptr, 1 if on else 0, int(wait_limit_ns)))
 
 
 def gptq_get_info(h: Handle) -> GptqInfo:
