@@ -77,13 +77,3 @@ def test_split_counters_reset_between_calls_and_graphs():
     torch.cuda.synchronize()
     for M in (40, 128):
         compare(ys[M].cpu(), oracle_y(ck, xs[M].cpu()))
-
-
-
-def test_small_path_never_splits():
-    spec = synth.LayerSpec(8192, 256, 4, 128, True, False, "fp16")
-    h = repack(synth.make_checkpoint(spec, seed=1))
-    gptq.gptq_reserve(h, 64)
-    for M in (1, 17, 28, 32):
-        assert gptq.gptq_gemm_k_splits(h, M, gptq.PATH_SMALL_M) == 1
-    assert gptq.gptq_gemm_k_splits(h, 64, gptq.PATH_AUTO) == gptq.gptq_gemm_k_splits(h, 64, gptq.PATH_LARGE_M)

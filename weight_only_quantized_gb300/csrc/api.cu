@@ -375,7 +375,7 @@ int gptq_gemm_k_splits(gptq_handle_t hh, int M, gptq_path_t path) {
   if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M) return -1;
   const Handle& h = *reinterpret_cast<const Handle*>(hh);
   if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
-  return path == GPTQ_PATH_LARGE_M ? large_split(h, M) : 1;     // the small-M kernel walks all of K
+  return path == GPTQ_PATH_LARGE_M ? large_split(h, M) : small_m_k_splits(h, M);
 }
 
 gptq_status_t gptq_destroy(gptq_handle_t hh) {

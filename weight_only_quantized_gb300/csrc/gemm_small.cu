@@ -273,7 +273,24 @@ struct SmallArgs {
   const float* bias;   // [Np] float32 added to y, or nullptr
   uint64_t wait_ns; // limit of every bounded wait
   int stall;        // test hook: the producer issues no copy, so every wait runs into its limit
+  int o_recv;       // SPLIT: the first CTA of a cluster receives the others' tile sums here,
+                    // [panel - 1][M][32] floats
 };
+
+// Thread-block cluster helpers (the K-split kernels).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(rank));
+  return d;
+}
+// 16 bytes into another CTA's shared memory, completing on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
 
 template <int CW>
 __device__ __forceinline__ void named_sync_consumers() {
@@ -282,7 +299,9 @@ __device__ __forceinline__ void named_sync_consumers() {
 
 // XS: the x sums of the CTA's first tile are kept (a table of NB * 8 * MT8 floats) for its later
 // tiles; false only in the layouts for very long K, where shared memory cannot hold the table.
-template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8, bool XS = true>
+// SPLIT: the CTA walks one K panel (blockIdx.y) of one tile, x of that panel staged once; the
+// panels of a tile form a thread-block cluster, and the first CTA adds up the others' sums.
+template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8, bool XS = true, bool SPLIT = false>
 __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
   static_assert(!FP8 || (BITS == 8 && !GATHER), "FP8 layers: 8-bit layout, x staged without gather");
   // the zero fold applies to integer codes; FP8 weights are their own values
@@ -297,8 +316,14 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int NB = a.Kr / 128;
-  const int T0 = (int)(((long)blockIdx.x * a.ntiles) / gridDim.x);
-  const int T1 = (int)(((long)(blockIdx.x + 1) * a.ntiles) / gridDim.x);
+  // Tile runs of ntiles / grid or one more; the first (ntiles % grid) CTAs take the longer runs.
+  // A CTA that needs a whole SM starts only when the previous call's CTA there has left, and CTAs
+  // start in index order as SMs free up, so the CTAs that start last have the shorter runs (the
+  // 70B gate layer at M = 1: 27.5 -> 26.5 us against runs spread evenly over the indices; kept as
+  // plain register arithmetic, since this kernel sits at its register limit).
+  const int t_base = a.ntiles / (int)gridDim.x, t_extra = a.ntiles % (int)gridDim.x;
+  const int T0 = (int)blockIdx.x * t_base + min((int)blockIdx.x, t_extra);
+  const int T1 = T0 + t_base + ((int)blockIdx.x < t_extra ? 1 : 0);
   const int lg = a.lg_rd, rd = 1 << lg;
 
   uint8_t* ring = smem;
@@ -313,6 +338,9 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   auto hfull = [&](int i) { return bar0 + 8u * (2 * rd + i); };
   auto hempty = [&](int i) { return bar0 + 8u * (2 * rd + 2 + i); };
   const uint32_t cgfull = bar0 + 8u * (2 * rd + 4);   // the chunk-group table has landed
+  // K panels this CTA walks: all of them, or (SPLIT) the one of blockIdx.y
+  const int p_lo = SPLIT ? (int)blockIdx.y : 0;
+  const int p_hi = SPLIT ? (int)blockIdx.y + 1 : a.npanel;
   const int32_t* pm = reinterpret_cast<const int32_t*>(smem + a.o_pm);
   uint8_t* rawx = smem + a.o_raw;
   const int zs_bytes = a.span_max * kZsRow;
@@ -324,6 +352,12 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), kSPB); }
     for (int i = 0; i < 2; ++i) { mbar_init(hfull(i), 1); mbar_init(hempty(i), kCW); }
     mbar_init(cgfull, 1);
+    if constexpr (SPLIT) {
+      // the first CTA of the cluster expects the other panels' sums of its tile
+      const uint32_t rbar = bar0 + 8u * (2 * rd + 5);
+      mbar_init(rbar, 1);
+      if (blockIdx.y == 0) mbar_arrive_expect_tx(rbar, (gridDim.y - 1) * (uint32_t)a.M * kTileN * 4u);
+    }
     fence_mbar_init();
   }
   // A CTA that owns a whole SM starts only when the previous call's CTA there has left, so its
@@ -333,6 +367,9 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   if (!a.cg_async)
     for (int i = tid; i < NB * 4; i += kThreadsS) cg[i] = __ldg(&a.cgid[i]);
   __syncthreads();
+  // every thread of the cluster arrives once here (after the barrier inits, which the release
+  // publishes to the cluster) and waits once before it exits or touches another CTA's memory
+  if constexpr (SPLIT) cluster_arrive();
 
   // Blocks of panel p, and the first group a panel touches (cgid ascends in the sorted order).
   auto panel_blocks = [&](int p) { return min(NB, (p + 1) * a.pb) - p * a.pb; };
@@ -357,7 +394,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     const bool cg_sent = a.cg_async && go != 0;
 
     for (int ti = T0; ti < T1; ++ti) {
-      for (int p = 0; p < a.npanel; ++p, ++q) {
+      for (int p = p_lo; p < p_hi; ++p, ++q) {
         const int nb = panel_blocks(p);
         const int hs = q & 1;
         if (q >= 2) mbar_wait_poison(hempty(hs), ((q >> 1) - 1) & 1, limit);
@@ -428,6 +465,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       mbar_wait_poison(hfull(qq & 1), (uint32_t)((qq >> 1) & 1), drain);
     if (cg_sent) mbar_wait_poison(cgfull, 0u, drain);
     if ((limit == 0 || drain == 0) && lane == 0) report_timeout(a.err);
+    if constexpr (SPLIT) cluster_wait();
     return;
   }
 
@@ -492,7 +530,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       for (int mt = 0; mt < MT8; ++mt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) { acc[i][mt][r] = 0.f; part[i][mt][r] = 0.f; xsp[mt][r] = 0.f; }
-    for (int p = 0; p < a.npanel; ++p, ++q) {
+    for (int p = p_lo; p < p_hi; ++p, ++q) {
       const int nb = panel_blocks(p);
       const int hs = q & 1;
       if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1), a.wait_ns)) ok = false;
@@ -500,10 +538,12 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
         // x[m][perm[j]] from the copied rows into the staged rows, two sorted rows per store (only
         // after the copy of perm has landed: after a timeout the indices would be garbage)
         if (ok) {
-          const int half = a.Kr / 2;
+          // pairs of sorted rows: all of them, or (SPLIT) those of this CTA's panel
+          const int i0 = SPLIT ? p * a.pb * 64 : 0;
+          const int half = SPLIT ? nb * 64 : a.Kr / 2;
           const uint16_t* rx = reinterpret_cast<const uint16_t*>(rawx);
           for (int i = tid; i < half; i += kCW * 32) {
-            const int k0 = pm[2 * i], k1 = pm[2 * i + 1];
+            const int k0 = pm[2 * (i0 + i)], k1 = pm[2 * (i0 + i) + 1];
             for (int m = 0; m < a.M; ++m) {
               const uint32_t lo = k0 >= 0 ? rx[(size_t)m * a.ldx + k0] : 0u;
               const uint32_t hi = k1 >= 0 ? rx[(size_t)m * a.ldx + k1] : 0u;
@@ -702,24 +742,77 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     named_sync_consumers<kCW>();
     if (!waited) { asm volatile("griddepcontrol.wait;" ::: "memory"); waited = true; }
     T* y = static_cast<T*>(a.y);
-    for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
-      const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+    // the CTA's sum of the tile: the warps' totals in warp order, per four columns
+    auto tile_sum = [&](const int ml, const int cl) {
       float4 sum = *reinterpret_cast<const float4*>(&red[ml * RS + cl]);
 #pragma unroll
       for (int w = 1; w < kCW; ++w) {
         const float4 v = *reinterpret_cast<const float4*>(&red[(size_t)w * MT8 * 8 * RS + ml * RS + cl]);
         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
       }
-      const int n = ti * kTileN + cl;
-      if (n < a.N) {   // N % 32 == 0: a group of 4 columns is all in or all out
-        if (a.bias) {
-          const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + n));
-          sum.x += b.x; sum.y += b.y; sum.z += b.z; sum.w += b.w;
+      return sum;
+    };
+    auto store_y = [&](const int ml, const int n, float4 sum) {
+      if (a.bias) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + n));
+        sum.x += b.x; sum.y += b.y; sum.z += b.z; sum.w += b.w;
+      }
+      uint2 o;
+      o.x = pack2<T>(sum.x, sum.y);
+      o.y = pack2<T>(sum.z, sum.w);
+      *reinterpret_cast<uint2*>(y + (size_t)ml * a.N + n) = o;
+    };
+    if constexpr (SPLIT) {
+      // The K panels of this tile are the CTAs of one cluster.  Every CTA but the first sends its
+      // sum of the tile into the first one's shared memory (st.async, completing on the first
+      // CTA's receive barrier) and is done; the first adds the partials in panel order (its own,
+      // then ranks 1, 2, ...) and stores y.  One cluster-wide barrier (passed long before, at the
+      // CTAs' start) orders the sends after the receive barrier's init; the receive is bounded.
+      cluster_wait();
+      const int rank = (int)blockIdx.y;
+      const uint32_t rbar = bar0 + 8u * (2 * rd + 5);
+      const uint32_t recv = smem_u32(smem + a.o_recv);
+      if (rank != 0) {
+        const uint32_t dst = cluster_map(recv, 0), dbar = cluster_map(rbar, 0);
+        for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+          const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+          st_async_f4(dst + (uint32_t)((((rank - 1) * a.M + ml) * kTileN + cl) * 4), tile_sum(ml, cl), dbar);
         }
-        uint2 o;
-        o.x = pack2<T>(sum.x, sum.y);
-        o.y = pack2<T>(sum.z, sum.w);
-        *reinterpret_cast<uint2*>(y + (size_t)ml * a.N + n) = o;
+      } else {
+        // always waited for (after a timeout too, with the drain's limit): the other CTAs write
+        // into this CTA's shared memory, so it must not exit while their sends are in flight
+        if (!mbar_wait(rbar, 0u, ok ? a.wait_ns : kWaitNs)) ok = false;
+        const float* rv = reinterpret_cast<const float*>(smem + a.o_recv);
+        for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+          const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+          float4 sum = tile_sum(ml, cl);
+          for (int r = 1; r < (int)gridDim.y; ++r) {
+            const float4 v = *reinterpret_cast<const float4*>(rv + ((r - 1) * a.M + ml) * kTileN + cl);
+            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+          }
+          if (ok) store_y(ml, ti * kTileN + cl, sum);   // a tile's 32 columns are all below N
+        }
+      }
+    } else {
+      for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+        const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+        float4 sum = *reinterpret_cast<const float4*>(&red[ml * RS + cl]);
+#pragma unroll
+        for (int w = 1; w < kCW; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(&red[(size_t)w * MT8 * 8 * RS + ml * RS + cl]);
+          sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        }
+        const int n = ti * kTileN + cl;
+        if (n < a.N) {   // N % 32 == 0: a group of 4 columns is all in or all out
+          if (a.bias) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + n));
+            sum.x += b.x; sum.y += b.y; sum.z += b.z; sum.w += b.w;
+          }
+          uint2 o;
+          o.x = pack2<T>(sum.x, sum.y);
+          o.y = pack2<T>(sum.z, sum.w);
+          *reinterpret_cast<uint2*>(y + (size_t)ml * a.N + n) = o;
+        }
       }
     }
   }
@@ -742,27 +835,61 @@ __global__ void k_gather_x(const uint16_t* __restrict__ x, const int32_t* __rest
 // Host plan: ints only, cached per handle and M.
 struct SmallPlan {
   int grid, ntiles, pb, npanel, single, lg_rd, span_max, x_row, o_x, o_zs, o_red, o_cg, o_xs, o_bar, smem, cw,
-      gather, o_pm, o_raw, cg_async, xs_on;
+      gather, o_pm, o_raw, cg_async, xs_on, split, o_recv;
 };
+
+// K split for layers with fewer 32-column tiles than SMs (M <= 8): the largest of 2, 4, 8 K panels
+// whose CTAs (one per tile and panel, a whole SM each; a tile's panels form one cluster) all fit on
+// the GPU at once, with at least two stages per panel; 1 = no split.  The split costs about a
+// microsecond (cluster launch and the partials' exchange) and saves ~0.06 us per 128-row block a
+// CTA no longer walks, so it is taken only when it saves at least 20 blocks per CTA (measured:
+// K = 4096 in two panels was 0.6 us slower, K = 8192 in two 0.3 us faster).
+int split_panels(const Handle& h, int M) {
+  if (M > 8) return 1;
+  const int NB = h.Kr / 128;
+  const int ntiles = (h.N + kTileN - 1) / kTileN;
+  int best = 1;
+  for (int sp = 2; sp <= 8; sp *= 2) {
+    if (ntiles * sp > h.sm_count) break;
+    const int pb = ((NB + sp - 1) / sp + kSPB - 1) / kSPB * kSPB;
+    if (pb < 2 * kSPB || (NB + pb - 1) / pb != sp) break;
+    best = sp;
+  }
+  if (best > 1 && NB * (best - 1) < 20 * best) best = 1;
+  return best;
+}
 
 // Layout for codes of `bits` bits and MT8 m-tiles; with_gather adds the perm copy.
 // level 0: the preferred layout; level >= 1 (when that does not fit, e.g. K of 64 Ki and more, whose
 // per-group header and per-block tables grow with K): 8 consumer warps, no x-sum table, and K
 // panels of at most NB >> (level - 1) blocks.
-bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p, int level = 0) {
+// split > 1: one CTA per tile and K panel of split panels (x of one panel staged once).
+bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p, int level = 0,
+                 int split = 1) {
   const int NB = h.Kr / 128;
   p.ntiles = (h.N + kTileN - 1) / kTileN;
-  p.grid = std::min(p.ntiles, h.sm_count);
+  p.grid = split > 1 ? p.ntiles : std::min(p.ntiles, h.sm_count);
+  p.split = split;
+  const int pb_split = ((NB + split - 1) / split + kSPB - 1) / kSPB * kSPB;
   // K-panel: all of K when x fits, else as many blocks as kXPanel holds (x double buffered)
-  const int x_all = M * (NB * 256 + 64);
+  const int x_all = M * ((split > 1 ? pb_split : NB) * 256 + 64);
   int target = kSmemFull;
   // A short CTA (x small, at most three tiles) takes half an SM and 8 consumer warps, so the next
   // call's CTA can start streaming beside it; a long one takes the whole SM, a deeper ring and
   // (at M <= 8) 16 consumer warps.
-  const bool short_cta = x_all <= kXSmall && (p.ntiles + p.grid - 1) / p.grid <= 3;
+  // (A CTA with a single tile takes the whole SM: its 16 warps finish the call's only tile sooner
+  // than 8 warps beside the next call's CTA would.)
+  const int tiles_per_cta = (p.ntiles + p.grid - 1) / p.grid;
+  const bool short_cta = split == 1 && x_all <= kXSmall && tiles_per_cta >= 2 && tiles_per_cta <= 3;
   p.cw = (mt8 == 1 && !short_cta && level == 0) ? 16 : 8;
+  if (split > 1 && p.cw != 16) return false;   // the split kernels are built with 16 consumer warps
   p.xs_on = level == 0 ? 1 : 0;
-  if (level == 0 && x_all <= kXSingle) {
+  if (split > 1) {
+    // one tile and one K panel per CTA, x of the panel staged once
+    if (level != 0 || x_all > kXSingle || (NB + pb_split - 1) / pb_split != split) return false;
+    p.single = 1;
+    p.pb = pb_split;
+  } else if (level == 0 && x_all <= kXSingle) {
     p.single = 1;
     p.pb = NB;
     if (short_cta) target = kSmemHalf;
@@ -790,7 +917,8 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const int xs_bytes = p.xs_on ? NB * 8 * mt8 * 4 : 0;   // x sums per block, reused by the later tiles
   const int pm_bytes = p.gather ? h.Kr * 4 : 0;
   const int raw_bytes = p.gather ? M * h.K * 2 : 0;
-  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + 5 * 8 + 16;
+  const int recv_bytes = split > 1 ? (split - 1) * M * kTileN * 4 : 0;   // the cluster's partial sums
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + recv_bytes + 6 * 8 + 16;
   const int SB = kSPB * bits * 512;
   int budget = target - fixed - 128;
   int rd = budget / (SB + 16);
@@ -816,8 +944,9 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   p.o_xs = p.o_cg + cg_bytes;
   p.o_pm = p.o_xs + xs_bytes;
   p.o_raw = p.o_pm + pm_bytes;
-  p.o_bar = p.o_raw + raw_bytes;
-  p.smem = p.o_bar + (2 * rdp + 5) * 8 + 128;     // + alignment slack of the base
+  p.o_recv = p.o_raw + raw_bytes;
+  p.o_bar = p.o_recv + recv_bytes;
+  p.smem = p.o_bar + (2 * rdp + 6) * 8 + 128;     // + alignment slack of the base
   return p.smem <= 227 * 1024;
 }
 
@@ -825,6 +954,12 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
 // weight ring keeps at least eight stages; otherwise a pre-pass gathers x into the workspace.
 bool make_plan(const Handle& h, int M, SmallPlan& p) {
   const int mt8 = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  const int split = split_panels(h, M);
+  if (split > 1) {
+    if (!h.identity && !h.fp8 && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p, 0, split) && p.gather && p.lg_rd >= 3)
+      return true;
+    if (plan_layout(h, M, h.bits, mt8, false, p, 0, split)) return true;
+  }
   if (!h.identity && !h.fp8 && M <= 2 && plan_layout(h, M, h.bits, mt8, true, p) && p.gather && p.lg_rd >= 3) return true;
   for (int level = 0; level <= 12; ++level)
     if (plan_layout(h, M, h.bits, mt8, false, p, level)) return true;
@@ -848,7 +983,9 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
         if constexpr (!FP8) {
           if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
           if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+          if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, true, false, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         }
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false, FP8, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       }
       if (e != cudaSuccess) return e;
       std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
@@ -860,9 +997,13 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   }
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   int ldx = h.K;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;   // K split: a tile's panels form one cluster
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = (unsigned)p.split;
+  attr[1].val.clusterDim.z = 1;
   if (!h.identity && !p.gather) {
     cudaLaunchConfig_t gcfg = {};
     const long total = (long)M * h.Kr;
@@ -880,17 +1021,23 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
   SmallArgs args{h.wr, h.cgid, h.zst, xs, y, h.err, ldx, M, h.N, h.Np, h.Kr, h.G,
                  p.ntiles, p.pb, p.npanel, p.single, p.lg_rd, p.span_max, p.x_row,
                  p.o_x, p.o_zs, p.o_red, p.o_cg, p.o_bar, p.o_xs, h.perm, p.gather, p.o_pm, p.o_raw, p.cg_async,
-                 h.zoff, h.has_bias ? h.bias : nullptr, h.wait_ns, h.test_stall};
+                 h.zoff, h.has_bias ? h.bias : nullptr, h.wait_ns, h.test_stall, p.o_recv};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
+  cfg.gridDim = dim3(p.grid, p.split);
   cfg.blockDim = dim3(p.cw == 16 ? threads_of<16>() : threads_of<8>());
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.split > 1 ? 2 : 1;
   if (!p.xs_on)   // the long-K layouts: 8 consumer warps, no gather, no x-sum table
     return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8, false>, args, h.wr_map);
   if constexpr (MT8 == 1) {
+    if (p.split > 1) {   // K split (planned only with 16 consumer warps and the x-sum table)
+      if (p.cw != 16 || !p.xs_on) return cudaErrorInvalidConfiguration;   // block size must match the kernel
+      if constexpr (!FP8)
+        if (p.gather) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true, false, true, true>, args, h.wr_map);
+      return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false, FP8, true, true>, args, h.wr_map);
+    }
     if constexpr (!FP8) {
       if (p.gather)
         return p.cw == 16 ? cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true, false>, args, h.wr_map)
@@ -935,10 +1082,15 @@ bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out) {
   out->consumer_warps = p.cw;
   out->m_tiles = M <= 8 ? 1 : M <= 16 ? 2 : 4;
   out->act_order_in_kernel = p.gather;
-  out->k_splits = 1;
+  out->k_splits = p.split;
   out->k_panels = p.npanel;
   out->stages = 1 << p.lg_rd;
   return true;
+}
+
+int small_m_k_splits(const Handle& h, int M) {
+  SmallPlan p{};
+  return (M >= 1 && M <= 32 && make_plan(h, M, p)) ? p.split : 1;
 }
 
 int small_m_launches(const Handle& h, int M) {

@@ -129,6 +129,7 @@ int large_tile_count(const Handle& h, int M);   // output tiles (x tile x 128 we
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
 int small_m_max();   // largest M the small-M kernel covers (four m-tiles of 8 rows)
+int small_m_k_splits(const Handle& h, int M);   // K panels the small-M kernel splits a call into (1 = none)
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
 bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out);   // false: no plan fits
 
