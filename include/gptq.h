@@ -242,8 +242,10 @@ gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gpt
 int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Number of K ranges a gptq_gemm_path call at this M is split into (1 = none): the large-M kernel
- * splits grids that would leave SMs idle, where gptq_reserve covered M; the small-M kernel never
- * splits.  -1 on a bad argument.  Host only. */
+ * splits grids that would leave SMs idle, where gptq_reserve covered M (partials in the reserved
+ * workspace); the small-M kernel splits layers with fewer 32-column tiles than SMs at M <= 8 when
+ * each CTA's work shrinks enough, with the K panels of a tile in one thread-block cluster (partials
+ * exchanged in shared memory, no workspace).  -1 on a bad argument.  Host only. */
 int gptq_gemm_k_splits(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Free the handle and everything it owns.  Waits for the device to finish using it
