@@ -484,6 +484,9 @@ def extra_workloads(args, hbm, tf_burst, peak_kind, tf_sus):
     s4, m4 = synth.workload(PREFILL)
     r4 = one(s4, [4096] if args.quick_prefill else [4096] + [m for m in m4 if m != 4096], 1)
     out["prefill_m4096"] = dict(r4.pop("M=4096"), workload=PREFILL)
+    tr = traffic_record("gemm_large.cu", PREFILL)
+    # DRAM bytes of one launch from the committed ncu capture (while the kernel code is unchanged)
+    out["prefill_m4096"]["traffic"] = tr["dram_bytes_per_launch"] if tr else None
     out[PREFILL] = r4
     out["awq-4096x14336-b4g128-fp16"] = awq_layer(hbm, tf_burst)
     out["fp8-4096x14336-block128-bf16"] = fp8_layer(hbm, tf_burst)
