@@ -535,20 +535,31 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       const int hs = q & 1;
       if (ok && !mbar_wait(hfull(hs), (uint32_t)((q >> 1) & 1), a.wait_ns)) ok = false;
       if (GATHER && q == 0) {
-        // x[m][perm[j]] from the copied rows into the staged rows, two sorted rows per store (only
-        // after the copy of perm has landed: after a timeout the indices would be garbage)
+        // x[m][perm[j]] from the copied rows into the staged rows (only after the copy of perm has
+        // landed: after a timeout the indices would be garbage).  One warp per 128-row block, lane l
+        // on the block's sorted rows 4l .. 4l + 3 (one 16-byte load of perm, one 8-byte store per x
+        // row); the warp also sums the block's x per batch row into the x-sum table, so that no tile
+        // needs the all-ones MMAs (columns of absent batch rows read row 0, as the fragments do).
         if (ok) {
-          // pairs of sorted rows: all of them, or (SPLIT) those of this CTA's panel
-          const int i0 = SPLIT ? p * a.pb * 64 : 0;
-          const int half = SPLIT ? nb * 64 : a.Kr / 2;
+          const int b0p = SPLIT ? p * a.pb : 0;     // blocks of this CTA's rows: all, or its panel's
+          const int nbp = SPLIT ? nb : NB;
           const uint16_t* rx = reinterpret_cast<const uint16_t*>(rawx);
-          for (int i = tid; i < half; i += kCW * 32) {
-            const int k0 = pm[2 * (i0 + i)], k1 = pm[2 * (i0 + i) + 1];
+          for (int bl = warp; bl < nbp; bl += kCW) {
+            const int b = b0p + bl;
+            const int4 kk = *reinterpret_cast<const int4*>(pm + 128 * b + 4 * lane);
+            float srow[2] = {0.f, 0.f};
             for (int m = 0; m < a.M; ++m) {
-              const uint32_t lo = k0 >= 0 ? rx[(size_t)m * a.ldx + k0] : 0u;
-              const uint32_t hi = k1 >= 0 ? rx[(size_t)m * a.ldx + k1] : 0u;
-              *reinterpret_cast<uint32_t*>(xreg + m * a.x_row + 4 * i) = lo | (hi << 16);
+              const uint16_t* xr = rx + (size_t)m * a.ldx;
+              const uint32_t v0 = kk.x >= 0 ? xr[kk.x] : 0u, v1 = kk.y >= 0 ? xr[kk.y] : 0u;
+              const uint32_t v2 = kk.z >= 0 ? xr[kk.z] : 0u, v3 = kk.w >= 0 ? xr[kk.w] : 0u;
+              *reinterpret_cast<uint2*>(xreg + m * a.x_row + 256 * bl + 8 * lane) =
+                  make_uint2(v0 | (v1 << 16), v2 | (v3 << 16));
+              float sm = (to_float<T>(v0) + to_float<T>(v1)) + (to_float<T>(v2) + to_float<T>(v3));
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+              srow[m & 1] = sm;
             }
+            if (XS && lane < 8 * MT8) xsb[(size_t)b * (8 * MT8) + lane] = (lane == 1 && a.M == 2) ? srow[1] : srow[0];
           }
         }
         named_sync_consumers<kCW>();      // every consumer's share of x is in place
@@ -717,7 +728,8 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           }
         }
       };
-      if (XS && ti > T0) run_blocks(std::true_type{});
+      if constexpr (XS && GATHER) run_blocks(std::true_type{});   // the permute wrote the x-sum table
+      else if (XS && ti > T0) run_blocks(std::true_type{});
       else run_blocks(std::false_type{});
       s_base += nst;
       __syncwarp();
