@@ -946,9 +946,14 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   while ((2 << p.lg_rd) <= rd) ++p.lg_rd;     // largest power of two <= rd
   const int rdp = 1 << p.lg_rd;
   // A consumer warp's consecutive stages are cw / kSPB apart.  A parity wait on a slot tells apart
-  // only the slot's current and previous phase, so the ring must hold at least that many stages
-  // (else a warp would wait two phases ahead on the same slot and read a stale stage).
-  if (rdp * kSPB < p.cw) return false;
+  // only the slot's current and previous phase, and that previous phase must be one the waiting
+  // warp has consumed itself: the ring depth must be a multiple of that distance (then the slot's
+  // previous stage is the warp's own earlier one, complete), which for the power-of-two rings and
+  // 8 or 16 consumer warps means at least that many stages.  (A ring that is not a multiple --
+  // 12 warps, 3 stages apart, on a 4-stage ring -- let a warp wait on a slot whose previous stage,
+  // taken by other warps, was still in flight, and read it as its own: bulk copies can complete
+  // out of order.)
+  if (rdp * kSPB < p.cw || rdp % (p.cw / kSPB) != 0) return false;
   p.o_x = rdp * SB;
   p.o_zs = p.o_x + (x_bytes + 15) / 16 * 16;
   p.o_red = p.o_zs + zs_bytes;
