@@ -889,10 +889,13 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   // A short CTA (x small, at most three tiles) takes half an SM and 8 consumer warps, so the next
   // call's CTA can start streaming beside it; a long one takes the whole SM, a deeper ring and
   // (at M <= 8) 16 consumer warps.
-  // (A CTA with a single tile takes the whole SM: its 16 warps finish the call's only tile sooner
-  // than 8 warps beside the next call's CTA would.)
+  // Measured: the half-SM shape wins only when the runs are nearly even (decode layer, 448 tiles on
+  // 152 CTAs: 8.9 vs 9.3 us at M = 1).  A CTA with a single tile, or runs where more than an eighth
+  // of the CTAs have one tile less, take the whole SM: 16 warps finish sooner than 8 beside the next
+  // call's CTA (K = 4096, N = 11008: 8.5 -> 7.9 us; K = N = 4096: 13-29 % faster).
   const int tiles_per_cta = (p.ntiles + p.grid - 1) / p.grid;
-  const bool short_cta = split == 1 && x_all <= kXSmall && tiles_per_cta >= 2 && tiles_per_cta <= 3;
+  const bool short_cta = split == 1 && x_all <= kXSmall && tiles_per_cta >= 2 && tiles_per_cta <= 3 &&
+                         p.ntiles >= tiles_per_cta * p.grid - p.grid / 8;
   p.cw = (mt8 == 1 && !short_cta && level == 0) ? 16 : 8;
   if (split > 1 && p.cw != 16) return false;   // the split kernels are built with 16 consumer warps
   p.xs_on = level == 0 ? 1 : 0;
