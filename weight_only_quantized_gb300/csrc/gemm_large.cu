@@ -294,11 +294,13 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   for (int i = tid; i < nchunks; i += kThreadsL) cg[i] = __ldg(&a.cgid[c0 + i]);
+  __syncthreads();
   // bit j of gmask[w]: chunk 32 w + j of the range is the last chunk of its group inside the range
-  // (the MMA issuer's schedule); the range's last chunk always closes one
+  // (the MMA issuer's schedule); the range's last chunk always closes one (from the shared copy:
+  // one global round trip fewer before the pipeline starts)
   for (int w0 = 32 * warp; w0 < nchunks; w0 += kThreadsL) {
     const int c = w0 + lane;
-    const bool end = c < nchunks && (c + 1 == nchunks || __ldg(&a.cgid[c0 + c + 1]) != __ldg(&a.cgid[c0 + c]));
+    const bool end = c < nchunks && (c + 1 == nchunks || cg[c + 1] != cg[c]);
     const uint32_t m = __ballot_sync(0xffffffffu, end);
     if (lane == 0) gmask[w0 / 32] = m;
   }
