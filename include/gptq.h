@@ -244,8 +244,9 @@ int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
 /* Number of K ranges a gptq_gemm_path call at this M is split into (1 = none): the large-M kernel
  * splits grids that would leave SMs idle, where gptq_reserve covered M (partials in the reserved
  * workspace); the small-M kernel splits layers with fewer 32-column tiles than SMs at M <= 8 when
- * each CTA's work shrinks enough, with the K panels of a tile in one thread-block cluster (partials
- * exchanged in shared memory, no workspace).  -1 on a bad argument.  Host only. */
+ * each CTA's work shrinks enough, and layers whose x over all of K does not fit in shared memory at
+ * M = 9 .. 16, with the K panels of a tile (or of a run of tiles) in one thread-block cluster
+ * (partials exchanged in shared memory, no workspace).  -1 on a bad argument.  Host only. */
 int gptq_gemm_k_splits(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Free the handle and everything it owns.  Waits for the device to finish using it
@@ -327,7 +328,7 @@ gptq_status_t gptq_repack_noalloc(const int32_t* qweight, const int32_t* qzeros,
 typedef struct {
   int path;            /* GPTQ_PATH_SMALL_M or GPTQ_PATH_LARGE_M                               */
   int launches;        /* kernels per call (an activation gather or permute counts as one)     */
-  int grid;            /* CTAs of the GEMM kernel                                               */
+  int grid;            /* CTAs of the GEMM kernel (K split: clusters of k_splits CTAs)          */
   int threads;         /* threads per CTA                                                       */
   int smem_bytes;      /* dynamic shared memory per CTA                                         */
   int consumer_warps;  /* small-M: warps that dequantise and multiply; large-M: 4 dequantisers  */

@@ -19,11 +19,13 @@ pytestmark = pytest.mark.gpu
 
 # (spec, M): a single-tile CTA (identity order); a 16-warp CTA with act-order x permuted in shared
 # memory; act-order with the gather pre-pass (which still runs normally); the K split, whose first
-# CTA of each cluster still waits for the other CTAs' sends after its own waits gave up
+# CTA of each cluster still waits for the other CTAs' sends after its own waits gave up; the K split
+# at two m-tiles, whose clusters still pass their tile sums through both receive slots
 CASES = [(synth.LayerSpec(1024, 512, 4, 128, False, False, "fp16"), 1),
          (synth.LayerSpec(512, 16384, 4, 128, True, False, "bf16"), 1),
          (synth.LayerSpec(512, 1024, 3, 64, True, False, "fp16"), 4),
-         (synth.LayerSpec(4096, 512, 4, 128, False, False, "bf16"), 1)]
+         (synth.LayerSpec(4096, 512, 4, 128, False, False, "bf16"), 1),
+         (synth.LayerSpec(8192, 8192, 4, 128, False, False, "bf16"), 16)]
 
 
 def _id(c):

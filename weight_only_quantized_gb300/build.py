@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 SO = os.path.join(LIBDIR, "libgptq_gb300.so")
-SOURCES = ["api.cu", "repack.cu", "gemm_small.cu", "gemm_large.cu"]
+SOURCES = ["api.cu", "repack.cu", "gemm_small.cu", "gemm_small_bf16.cu", "gemm_large.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

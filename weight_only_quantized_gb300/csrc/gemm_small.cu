@@ -273,8 +273,8 @@ struct SmallArgs {
   const float* bias;   // [Np] float32 added to y, or nullptr
   uint64_t wait_ns; // limit of every bounded wait
   int stall;        // test hook: the producer issues no copy, so every wait runs into its limit
-  int o_recv;       // SPLIT: the first CTA of a cluster receives the others' tile sums here,
-                    // [panel - 1][M][32] floats
+  int o_recv;       // SPLIT: two receive slots in the first CTA of a cluster for the other CTAs'
+                    // tile sums, [2][panels - 1][M][32] floats, then its own sums [2][M][32]
 };
 
 // Thread-block cluster helpers (the K-split kernels).
@@ -285,6 +285,30 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t ran
   uint32_t d;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(rank));
   return d;
+}
+// Arrive on an mbarrier of another CTA of the cluster, relaxed: no fence.  The caller issues it after
+// a barrier of the CTA's threads that read the slot being freed, and bar.sync completes their
+// shared-memory loads (their values are bound before it), so the other CTA's next writes into the
+// slot cannot reach a read.  A release arrive at cluster scope cost ~0.5 us per tile here.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+// Bounded parity wait on this CTA's mbarrier for a phase that another CTA of the cluster completes
+// (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(r) : "r"(bar), "r"(parity) : "memory");
+  return r != 0u;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_cluster(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
 }
 // 16 bytes into another CTA's shared memory, completing on that CTA's mbarrier.
 __device__ __forceinline__ void st_async_f4(uint32_t dst, float4 v, uint32_t bar) {
@@ -299,8 +323,8 @@ __device__ __forceinline__ void named_sync_consumers() {
 
 // XS: the x sums of the CTA's first tile are kept (a table of NB * 8 * MT8 floats) for its later
 // tiles; false only in the layouts for very long K, where shared memory cannot hold the table.
-// SPLIT: the CTA walks one K panel (blockIdx.y) of one tile, x of that panel staged once; the
-// panels of a tile form a thread-block cluster, and the first CTA adds up the others' sums.
+// SPLIT: the CTA walks one K panel (blockIdx.y) of each tile of its run, x of that panel staged
+// once; the panels form a thread-block cluster, and the first CTA adds up the others' sums.
 template <typename T, int BITS, int MT8, int CW, bool GATHER, bool FP8, bool XS = true, bool SPLIT = false>
 __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 1) k_gemm_small(const SmallArgs a, const __grid_constant__ CUtensorMap wmap) {
   static_assert(!FP8 || (BITS == 8 && !GATHER), "FP8 layers: 8-bit layout, x staged without gather");
@@ -338,6 +362,10 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
   auto hfull = [&](int i) { return bar0 + 8u * (2 * rd + i); };
   auto hempty = [&](int i) { return bar0 + 8u * (2 * rd + 2 + i); };
   const uint32_t cgfull = bar0 + 8u * (2 * rd + 4);   // the chunk-group table has landed
+  // SPLIT: receive slot s of the first CTA is full (the other CTAs' sums of one tile have landed),
+  // and, in every other CTA, slot s of the first CTA is free again
+  auto rbar = [&](int s) { return bar0 + 8u * (2 * rd + 5 + s); };
+  auto sfree = [&](int s) { return bar0 + 8u * (2 * rd + 7 + s); };
   // K panels this CTA walks: all of them, or (SPLIT) the one of blockIdx.y
   const int p_lo = SPLIT ? (int)blockIdx.y : 0;
   const int p_hi = SPLIT ? (int)blockIdx.y + 1 : a.npanel;
@@ -352,11 +380,17 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
     for (int i = 0; i < rd; ++i) { mbar_init(full(i), 1); mbar_init(empty(i), kSPB); }
     for (int i = 0; i < 2; ++i) { mbar_init(hfull(i), 1); mbar_init(hempty(i), kCW); }
     mbar_init(cgfull, 1);
-    if constexpr (SPLIT) {
+    if constexpr (SPLIT && MT8 == 1) {
       // the first CTA of the cluster expects the other panels' sums of its tile
-      const uint32_t rbar = bar0 + 8u * (2 * rd + 5);
-      mbar_init(rbar, 1);
-      if (blockIdx.y == 0) mbar_arrive_expect_tx(rbar, (gridDim.y - 1) * (uint32_t)a.M * kTileN * 4u);
+      mbar_init(rbar(0), 1);
+      if (blockIdx.y == 0) mbar_arrive_expect_tx(rbar(0), (gridDim.y - 1) * (uint32_t)a.M * kTileN * 4u);
+    } else if constexpr (SPLIT) {
+      // the first CTA of the cluster expects the other panels' sums of its first two tiles (one
+      // slot each) and re-arms a slot when it has added it up
+      for (int sl = 0; sl < 2; ++sl) { mbar_init(rbar(sl), 1); mbar_init(sfree(sl), 1); }
+      if (blockIdx.y == 0)
+        for (int sl = 0; sl < 2 && sl < T1 - T0; ++sl)
+          mbar_arrive_expect_tx(rbar(sl), (gridDim.y - 1) * (uint32_t)a.M * kTileN * 4u);
     }
     fence_mbar_init();
   }
@@ -465,7 +499,11 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       mbar_wait_poison(hfull(qq & 1), (uint32_t)((qq >> 1) & 1), drain);
     if (cg_sent) mbar_wait_poison(cgfull, 0u, drain);
     if ((limit == 0 || drain == 0) && lane == 0) report_timeout(a.err);
-    if constexpr (SPLIT) cluster_wait();
+    if constexpr (SPLIT) {
+      cluster_wait();
+      if constexpr (MT8 > 1)   // runs of tiles (one tile per cluster at M <= 8)
+        if (T1 - T0 > 1) { cluster_arrive(); cluster_wait(); }   // the cluster's closing barrier
+    }
     return;
   }
 
@@ -774,18 +812,17 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       o.y = pack2<T>(sum.z, sum.w);
       *reinterpret_cast<uint2*>(y + (size_t)ml * a.N + n) = o;
     };
-    if constexpr (SPLIT) {
-      // The K panels of this tile are the CTAs of one cluster.  Every CTA but the first sends its
-      // sum of the tile into the first one's shared memory (st.async, completing on the first
-      // CTA's receive barrier) and is done; the first adds the partials in panel order (its own,
-      // then ranks 1, 2, ...) and stores y.  One cluster-wide barrier (passed long before, at the
-      // CTAs' start) orders the sends after the receive barrier's init; the receive is bounded.
+    if constexpr (SPLIT && MT8 == 1) {
+      // M <= 8: one tile per cluster.  Every CTA but the first sends its sum of the tile into the
+      // first one's shared memory (st.async, completing on the first CTA's receive barrier) and is
+      // done; the first adds the partials in panel order (its own, then ranks 1, 2, ...) and stores
+      // y.  One cluster-wide barrier (passed long before, at the CTAs' start) orders the sends
+      // after the receive barrier's init; the receive is bounded.
       cluster_wait();
       const int rank = (int)blockIdx.y;
-      const uint32_t rbar = bar0 + 8u * (2 * rd + 5);
       const uint32_t recv = smem_u32(smem + a.o_recv);
       if (rank != 0) {
-        const uint32_t dst = cluster_map(recv, 0), dbar = cluster_map(rbar, 0);
+        const uint32_t dst = cluster_map(recv, 0), dbar = cluster_map(rbar(0), 0);
         for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
           const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
           st_async_f4(dst + (uint32_t)((((rank - 1) * a.M + ml) * kTileN + cl) * 4), tile_sum(ml, cl), dbar);
@@ -793,7 +830,7 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       } else {
         // always waited for (after a timeout too, with the drain's limit): the other CTAs write
         // into this CTA's shared memory, so it must not exit while their sends are in flight
-        if (!mbar_wait(rbar, 0u, ok ? a.wait_ns : kWaitNs)) ok = false;
+        if (!mbar_wait(rbar(0), 0u, ok ? a.wait_ns : kWaitNs)) ok = false;
         const float* rv = reinterpret_cast<const float*>(smem + a.o_recv);
         for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
           const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
@@ -804,6 +841,69 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
           }
           if (ok) store_y(ml, ti * kTileN + cl, sum);   // a tile's 32 columns are all below N
         }
+      }
+    } else if constexpr (SPLIT) {
+      // M = 9 .. 16: the K panels of the run's tiles are the CTAs of one cluster.  Every CTA but
+      // the first sends its sum of each tile into one of two receive slots in the first CTA's
+      // shared memory (st.async, completing on that slot's receive barrier).  The first CTA keeps
+      // its own sum and adds tile i up (its own, then ranks 1, 2, ... in order) after its own sum
+      // of tile i + 1, so that the exchange is off its way; then it re-arms the slot and arrives on
+      // the other CTAs' slot-free barriers, which they wait for before they send tile i + 2 into
+      // it.  The cluster barrier passed at the first tile orders every send and remote arrive
+      // after the barriers' init; every wait is bounded.
+      static_assert(MT8 * 8 * (kTileN / 4) < kCW * 32, "one tile sum float4 per thread, the last thread free");
+      const int it = ti - T0, run = T1 - T0, slot = it & 1;
+      const int rank = (int)blockIdx.y, nsend = (int)gridDim.y - 1;
+      const int per = a.M * kTileN;                 // floats of one tile sum
+      float* recv = reinterpret_cast<float*>(smem + a.o_recv);
+      float* own = recv + 2 * nsend * per;
+      if (it == 0) cluster_wait();
+      if (rank != 0) {
+        if (it >= 2 && !mbar_wait_cluster(sfree(slot), (uint32_t)(((it >> 1) - 1) & 1), ok ? a.wait_ns : kWaitNs))
+          ok = false;
+        // (sent after a timeout too: the first CTA counts on every send of every tile)
+        const uint32_t dst = cluster_map(smem_u32(recv + (slot * nsend + rank - 1) * per), 0);
+        const uint32_t dbar = cluster_map(rbar(slot), 0);
+        for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+          const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+          st_async_f4(dst + (uint32_t)((ml * kTileN + cl) * 4), tile_sum(ml, cl), dbar);
+        }
+      } else {
+        for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
+          const int ml = i / (kTileN / 4), cl = 4 * (i % (kTileN / 4));
+          *reinterpret_cast<float4*>(own + slot * per + ml * kTileN + cl) = tile_sum(ml, cl);
+        }
+        auto finish = [&](const int j) {
+          const int sj = j & 1;
+          // always waited for (after a timeout too, with the drain's limit): the other CTAs write
+          // into this CTA's shared memory, so it must not exit while their sends are in flight
+          if (!mbar_wait(rbar(sj), (uint32_t)((j >> 1) & 1), ok ? a.wait_ns : kWaitNs)) ok = false;
+          // one float4 of the tile per thread, in the first half of the consumer threads (each
+          // reads back only the own sum it wrote itself)
+          const bool mine = tid < a.M * (kTileN / 4);
+          const int ml = tid / (kTileN / 4), cl = 4 * (tid % (kTileN / 4));
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (mine) {
+            sum = *reinterpret_cast<const float4*>(own + sj * per + ml * kTileN + cl);
+            for (int r = 0; r < nsend; ++r) {
+              const float4 v = *reinterpret_cast<const float4*>(recv + (sj * nsend + r) * per + ml * kTileN + cl);
+              sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+          }
+          if (j + 2 < run) {
+            named_sync_consumers<kCW>();             // every consumer has read slot sj
+            // The last consumer thread frees the slot: it stores no y (from thread 0, with the y
+            // stores before it, the arrive held warp 0 ~1 us per tile, and every warp then waited
+            // for warp 0 at the next tile).
+            if (tid == kCW * 32 - 1) {
+              mbar_arrive_expect_tx(rbar(sj), (uint32_t)(nsend * per) * 4u);
+              for (int r = 1; r <= nsend; ++r) mbar_arrive_remote(cluster_map(sfree(sj), (uint32_t)r));
+            }
+          }
+          if (mine && ok) store_y(ml, (T0 + j) * kTileN + cl, sum);   // a tile's 32 columns are all below N
+        };
+        if (it >= 1) finish(it - 1);
+        if (it == run - 1) finish(it);
       }
     } else {
       for (int i = tid; i < a.M * (kTileN / 4); i += kCW * 32) {
@@ -828,6 +928,8 @@ __global__ void __launch_bounds__(threads_of<CW>(), (CW == 8 && MT8 == 1) ? 2 : 
       }
     }
   }
+  if constexpr (SPLIT && MT8 > 1)
+    if (T1 - T0 > 1) { cluster_arrive(); cluster_wait(); }   // the cluster's closing barrier
   if (!ok) report_timeout(a.err);
 }
 
@@ -850,19 +952,71 @@ struct SmallPlan {
       gather, o_pm, o_raw, cg_async, xs_on, split, o_recv;
 };
 
+// This file is compiled twice: as itself (fp16 layers and the plan queries) and, through
+// gemm_small_bf16.cu, for bf16 layers, so that the two halves of the kernel instantiations build in
+// parallel.
+#ifdef GPTQ_SMALL_BF16_UNIT
+using UnitT = __nv_bfloat16;
+#else
+using UnitT = __half;
+#endif
+
+// Clusters of S CTAs that take a whole SM each and that the GPU runs at once.  One kernel built for
+// clusters answers for all of them: at one CTA per SM the count depends only on the cluster size
+// and on how the SMs are grouped.
+int whole_sm_clusters(const Handle& h, int S) {
+  const int idx = S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : 0;
+  if (idx == 0) return h.sm_count;
+  int n = h.clusters_fit[idx].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  auto fn = k_gemm_small<UnitT, 4, 2, 8, false, false, true, true>;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = (unsigned)S;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, (unsigned)S);
+  cfg.blockDim = dim3(threads_of<8>());
+  cfg.dynamicSmemBytes = kSmemFull;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemFull) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = h.sm_count / S;
+  }
+  n = std::max(1, std::min(n, h.sm_count / S));
+  h.clusters_fit[idx].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 // K split for layers with fewer 32-column tiles than SMs (M <= 8): the largest of 2, 4, 8 K panels
-// whose CTAs (one per tile and panel, a whole SM each; a tile's panels form one cluster) all fit on
-// the GPU at once, with at least two stages per panel; 1 = no split.  The split costs about a
+// whose CTAs (one per tile and panel, a whole SM each; a tile's panels form one cluster) all run
+// at once, with at least two stages per panel; 1 = no split.  The split costs about a
 // microsecond (cluster launch and the partials' exchange) and saves ~0.06 us per 128-row block a
 // CTA no longer walks, so it is taken only when it saves at least 20 blocks per CTA (measured:
 // K = 4096 in two panels was 0.6 us slower, K = 8192 in two 0.3 us faster).
+//
+// M = 9 .. 16 (two m-tiles), when x over all of K is too large to stage once: the fewest of 2, 4, 8
+// K panels whose x fits, each CTA of a cluster walking its panel of every tile of the cluster's
+// run, so x is staged once per CTA instead of once per tile and panel (the 70B gate layer at
+// M = 16: 67.9 us with x staged per panel; the same per-CTA work with x staged once, 38.9 us).
 int split_panels(const Handle& h, int M) {
-  if (M > 8) return 1;
   const int NB = h.Kr / 128;
   const int ntiles = (h.N + kTileN - 1) / kTileN;
+  if (M > 8) {
+    if (M > 16 || M * (NB * 256 + 64) <= kXSingle) return 1;
+    for (int sp = 2; sp <= 8; sp *= 2) {
+      const int pb = ((NB + sp - 1) / sp + kSPB - 1) / kSPB * kSPB;
+      if (pb < 2 * kSPB || (NB + pb - 1) / pb != sp) return 1;
+      if (M * (pb * 256 + 64) <= kXSingle) return sp;
+    }
+    return 1;
+  }
   int best = 1;
   for (int sp = 2; sp <= 8; sp *= 2) {
-    if (ntiles * sp > h.sm_count) break;
+    if (ntiles > whole_sm_clusters(h, sp)) break;
     const int pb = ((NB + sp - 1) / sp + kSPB - 1) / kSPB * kSPB;
     if (pb < 2 * kSPB || (NB + pb - 1) / pb != sp) break;
     best = sp;
@@ -875,12 +1029,13 @@ int split_panels(const Handle& h, int M) {
 // level 0: the preferred layout; level >= 1 (when that does not fit, e.g. K of 64 Ki and more, whose
 // per-group header and per-block tables grow with K): 8 consumer warps, no x-sum table, and K
 // panels of at most NB >> (level - 1) blocks.
-// split > 1: one CTA per tile and K panel of split panels (x of one panel staged once).
+// split > 1: clusters of `split` CTAs, one per K panel, over runs of tiles (x of one panel staged
+// once).
 bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, SmallPlan& p, int level = 0,
                  int split = 1) {
   const int NB = h.Kr / 128;
   p.ntiles = (h.N + kTileN - 1) / kTileN;
-  p.grid = split > 1 ? p.ntiles : std::min(p.ntiles, h.sm_count);
+  p.grid = split > 1 ? std::min(p.ntiles, whole_sm_clusters(h, split)) : std::min(p.ntiles, h.sm_count);
   p.split = split;
   const int pb_split = ((NB + split - 1) / split + kSPB - 1) / kSPB * kSPB;
   // K-panel: all of K when x fits, else as many blocks as kXPanel holds (x double buffered)
@@ -897,7 +1052,8 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const bool short_cta = split == 1 && x_all <= kXSmall && tiles_per_cta >= 2 && tiles_per_cta <= 3 &&
                          p.ntiles >= tiles_per_cta * p.grid - p.grid / 8;
   p.cw = (mt8 == 1 && !short_cta && level == 0) ? 16 : 8;
-  if (split > 1 && p.cw != 16) return false;   // the split kernels are built with 16 consumer warps
+  // the split kernels: 16 consumer warps for one m-tile, 8 for two
+  if (split > 1 && (mt8 > 2 || p.cw != (mt8 == 1 ? 16 : 8))) return false;
   p.xs_on = level == 0 ? 1 : 0;
   if (split > 1) {
     // one tile and one K panel per CTA, x of the panel staged once
@@ -932,8 +1088,9 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const int xs_bytes = p.xs_on ? NB * 8 * mt8 * 4 : 0;   // x sums per block, reused by the later tiles
   const int pm_bytes = p.gather ? h.Kr * 4 : 0;
   const int raw_bytes = p.gather ? M * h.K * 2 : 0;
-  const int recv_bytes = split > 1 ? (split - 1) * M * kTileN * 4 : 0;   // the cluster's partial sums
-  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + recv_bytes + 6 * 8 + 16;
+  // the cluster's partial sums: two receive slots of the other CTAs' sums and two of the CTA's own
+  const int recv_bytes = split > 1 ? 2 * split * M * kTileN * 4 : 0;
+  const int fixed = x_bytes + zs_bytes + red_bytes + cg_bytes + xs_bytes + pm_bytes + raw_bytes + recv_bytes + 9 * 8 + 16;
   const int SB = kSPB * bits * 512;
   int budget = target - fixed - 128;
   int rd = budget / (SB + 16);
@@ -966,7 +1123,7 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   p.o_raw = p.o_pm + pm_bytes;
   p.o_recv = p.o_raw + raw_bytes;
   p.o_bar = p.o_recv + recv_bytes;
-  p.smem = p.o_bar + (2 * rdp + 6) * 8 + 128;     // + alignment slack of the base
+  p.smem = p.o_bar + (2 * rdp + 9) * 8 + 128;     // + alignment slack of the base
   return p.smem <= 227 * 1024;
 }
 
@@ -1007,6 +1164,8 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
         }
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 16, false, FP8, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       }
+      if constexpr (MT8 == 2)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_small<T, BITS, MT8, 8, false, FP8, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
       if (e != cudaSuccess) return e;
       std::vector<int64_t> v((sizeof(SmallPlan) + 7) / 8, 0);
       std::memcpy(v.data(), &p, sizeof(SmallPlan));
@@ -1053,7 +1212,8 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
     return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8, false>, args, h.wr_map);
   if constexpr (MT8 == 1) {
     if (p.split > 1) {   // K split (planned only with 16 consumer warps and the x-sum table)
-      if (p.cw != 16 || !p.xs_on) return cudaErrorInvalidConfiguration;   // block size must match the kernel
+      // block size must match the kernel, and this kernel ends one tile per cluster
+      if (p.cw != 16 || !p.xs_on || p.grid != p.ntiles) return cudaErrorInvalidConfiguration;
       if constexpr (!FP8)
         if (p.gather) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, true, false, true, true>, args, h.wr_map);
       return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false, FP8, true, true>, args, h.wr_map);
@@ -1064,7 +1224,13 @@ cudaError_t launch_t(const Handle& h, const void* x, void* y, int M, cudaStream_
                           : cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, true, false>, args, h.wr_map);
     }
     if (p.cw == 16) return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 16, false, FP8>, args, h.wr_map);
+  } else if constexpr (MT8 == 2) {
+    if (p.split > 1) {   // K split at two m-tiles: 8 consumer warps, x staged by the gather pre-pass
+      if (p.cw != 8 || p.gather) return cudaErrorInvalidConfiguration;
+      return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8, true, true>, args, h.wr_map);
+    }
   }
+  if (p.split > 1 || p.cw != 8) return cudaErrorInvalidConfiguration;   // no kernel built for that plan
   return cudaLaunchKernelEx(&cfg, k_gemm_small<T, BITS, MT8, 8, false, FP8>, args, h.wr_map);
 }
 
@@ -1089,6 +1255,7 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 
 }  // namespace
 
+#ifndef GPTQ_SMALL_BF16_UNIT
 int small_m_max() { return 32; }
 
 bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out) {
@@ -1121,8 +1288,13 @@ int small_m_launches(const Handle& h, int M) {
 }
 
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
-  if (h.dtype == GPTQ_BF16) return launch_dtype<__nv_bfloat16>(h, x, y, M, st);
+  if (h.dtype == GPTQ_BF16) return launch_gemm_small_bf16(h, x, y, M, st);
   return launch_dtype<__half>(h, x, y, M, st);
 }
+#else
+cudaError_t launch_gemm_small_bf16(const Handle& h, const void* x, void* y, int M, cudaStream_t st) {
+  return launch_dtype<__nv_bfloat16>(h, x, y, M, st);
+}
+#endif
 
 }  // namespace gptq

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
 #include <mutex>
@@ -67,6 +68,10 @@ struct Handle {
   // Launch plans by (path, M): computed once, so a call costs one kernel launch on the host.
   mutable std::mutex plan_mu;
   mutable std::unordered_map<int64_t, std::vector<int64_t>> plans;
+  // Thread-block clusters of 2, 4 and 8 whole-SM CTAs that the GPU holds at once (index log2 of
+  // the size; 0: not queried yet).  The SMs pair up by TPC and group by GPC, so a cluster size
+  // that does not divide a GPC's SMs leaves some of them idle.
+  mutable std::atomic<int> clusters_fit[4] = {0, 0, 0, 0};
 };
 
 // 128-row blocks fetched by one TMA box of the small-M kernel.
@@ -131,6 +136,7 @@ int small_m_launches(const Handle& h, int M);
 int small_m_max();   // largest M the small-M kernel covers (four m-tiles of 8 rows)
 int small_m_k_splits(const Handle& h, int M);   // K panels the small-M kernel splits a call into (1 = none)
 cudaError_t launch_gemm_small(const Handle& h, const void* x, void* y, int M, cudaStream_t st);
+cudaError_t launch_gemm_small_bf16(const Handle& h, const void* x, void* y, int M, cudaStream_t st);   // bf16 layers
 bool small_m_plan_info(const Handle& h, int M, gptq_plan_t* out);   // false: no plan fits
 
 // Large-M path: tcgen05 / TMEM / TMA kernel (plus an x-permute pre-pass when not identity).
