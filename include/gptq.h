@@ -117,18 +117,15 @@ gptq_status_t gptq_repack(const int32_t* qweight, const int32_t* qzeros, const v
 /*
  * Make gptq_gemm calls with M <= max_M possible without any allocation inside gptq_gemm.
  * This is the caller-owned scratch contract of GPTQModel "Kernel Backends Reference", section
- * "Marlin and caller-owned scratch" (the scratch API and its property table): the workspace
- * (reduction partials, permuted activations, a zeroed counter array) is sized by a query-free
- * reserve made before any graph capture, is owned by one stream at a time, and a call never falls
- * back to allocating when it is too small -- it fails (WORKSPACE) instead.
- * Only a handle whose g_idx order is not the identity (act-order, or groups whose sizes are
- * not multiples of 32) needs workspace above M = 32: max_M * K_sorted activation elements for
- * the permuted copy of x that the kernels read.  It also sizes the large-M kernel's K-split
- * workspace for every M <= max_M whose grid would leave SMs idle (fewer tiles than SMs, or a
- * mostly empty last wave): fp32 partials of at most 64 MB and one int32 counter per output tile.
- * Calls with an M this has not covered run without a K split (same results, slower at those M).
- * Allocates (cudaMalloc) outside any stream capture; never shrinks; the handle's device must be
- * current.  Errors: INVALID_ARG, CUDA.
+ * "Marlin and caller-owned scratch" (the scratch API and its property table): the workspace is
+ * sized by a query-free reserve made before any graph capture, is owned by one stream at a time,
+ * and a call never falls back to allocating when it is too small -- it fails (WORKSPACE) instead.
+ * The page's scratch also holds reduction partials and a zeroed counter array; here the K splits
+ * of both kernels keep their partials in the shared memory of a thread-block cluster, so the only
+ * workspace is the permuted copy of x.  Only a handle whose g_idx order is not the identity
+ * (act-order, or groups whose sizes are not multiples of 32) needs it above M = 32: max_M *
+ * K_sorted activation elements.  Allocates (cudaMalloc) outside any stream capture; never shrinks;
+ * the handle's device must be current.  Errors: INVALID_ARG, CUDA.
  */
 gptq_status_t gptq_reserve(gptq_handle_t h, int max_M);
 
@@ -242,8 +239,8 @@ gptq_status_t gptq_gemm_path(gptq_handle_t h, const void* x, void* y, int M, gpt
 int gptq_gemm_launches(gptq_handle_t h, int M, gptq_path_t path);
 
 /* Number of K ranges a gptq_gemm_path call at this M is split into (1 = none): the large-M kernel
- * splits grids that would leave SMs idle, where gptq_reserve covered M (partials in the reserved
- * workspace); the small-M kernel splits layers with fewer 32-column tiles than SMs at M <= 8 when
+ * splits grids that would leave SMs idle or a last wave mostly empty, the ranges of an output tile
+ * in one thread-block cluster; the small-M kernel splits layers with fewer 32-column tiles than SMs at M <= 8 when
  * each CTA's work shrinks enough, and layers whose x over all of K does not fit in shared memory at
  * M = 9 .. 16, with the K panels of a tile (or of a run of tiles) in one thread-block cluster
  * (partials exchanged in shared memory, no workspace).  -1 on a bad argument.  Host only. */

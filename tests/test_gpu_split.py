@@ -1,5 +1,7 @@
-"""GPU parity of the large-M kernel's K split (partials per K range, summed by the last CTA of each
-tile in a fixed order) against the oracle, on layers whose grid would leave SMs idle."""
+"""GPU parity of the large-M kernel's K split against the oracle, on layers whose grid would leave
+SMs idle: the K ranges of an output tile are the CTAs of one thread-block cluster, each keeps its
+fp32 partial in its shared memory, and CTA z sums the z-th slice of the tile's rows over all ranges
+in range order (distributed shared memory reads)."""
 import numpy as np
 import pytest
 import torch
@@ -29,9 +31,11 @@ def _id(s):
 def test_split_parity_and_determinism(spec, M):
     ck = synth.make_checkpoint(spec, seed=spec.K + M)
     h = repack(ck)
-    assert gptq.gptq_gemm_k_splits(h, M) == 1          # nothing reserved for the large path yet
-    gptq.gptq_reserve(h, 300)
-    assert gptq.gptq_gemm_k_splits(h, M) > 1
+    splits = gptq.gptq_gemm_k_splits(h, M, gptq.PATH_LARGE_M)
+    assert splits > 1                                   # no workspace needed for the split
+    gptq.gptq_reserve(h, 300)                           # (act-order: the permuted x above M = 32)
+    assert gptq.gptq_gemm_k_splits(h, M, gptq.PATH_LARGE_M) == splits
+    assert gptq.gptq_gemm_plan(h, M, gptq.PATH_LARGE_M).k_splits == splits
     x = synth.make_x(M, spec.K, spec.dtype, seed=M)
     y1 = run_gemm(h, x, spec.N, gptq.PATH_LARGE_M)
     compare(y1, oracle_y(ck, x))
@@ -43,7 +47,6 @@ def test_split_with_bias_awq_and_fp8():
     b = torch.randn(N, generator=torch.Generator().manual_seed(2)) * 0.1
     ck = synth.make_awq_checkpoint(K, N, 128, "fp16", seed=3)
     h = gptq.gptq_repack_awq(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(), 128)
-    gptq.gptq_reserve(h, 64)
     gptq.gptq_set_bias(h, b.half().cuda())
     assert gptq.gptq_gemm_k_splits(h, 64) > 1
     x = synth.make_x(64, K, "fp16", seed=4)
@@ -51,19 +54,18 @@ def test_split_with_bias_awq_and_fp8():
     compare(run_gemm(h, x, N, gptq.PATH_LARGE_M), y_ref)
     f8 = synth.make_fp8_checkpoint(K, N, "bf16", seed=5)
     h8 = gptq.gptq_repack_fp8(f8.weight.cuda(), f8.scale_inv.cuda(), torch.bfloat16)
-    gptq.gptq_reserve(h8, 64)
     assert gptq.gptq_gemm_k_splits(h8, 64) > 1
     x8 = synth.make_x(64, K, "bf16", seed=6)
     compare(run_gemm(h8, x8, N, gptq.PATH_LARGE_M), oracle.fp8_linear(f8.weight, f8.scale_inv, "bf16", x8))
 
 
-def test_split_counters_reset_between_calls_and_graphs():
-    """Many calls in a row, alternating M and captured in a CUDA graph: every result stays right, so
-    every tile counter returns to zero after each call."""
+def test_split_back_to_back_calls_and_graphs():
+    """Many calls in a row, alternating M and captured in a CUDA graph (the next call's clusters start
+    while this call's finish): every result stays right."""
     spec = synth.LayerSpec(4096, 256, 4, 128, False, False, "bf16")
     ck = synth.make_checkpoint(spec, seed=7)
     h = repack(ck)
-    gptq.gptq_reserve(h, 128)
+    assert gptq.gptq_gemm_k_splits(h, 40) > 1 and gptq.gptq_gemm_k_splits(h, 128) > 1
     xs = {M: synth.make_x(M, spec.K, "bf16", seed=M).cuda() for M in (40, 128)}
     ys = {M: torch.empty(M, spec.N, dtype=torch.bfloat16, device="cuda") for M in xs}
     torch.cuda.synchronize()

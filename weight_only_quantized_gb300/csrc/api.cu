@@ -49,8 +49,6 @@ static void free_handle(Handle* h) {
   cudaFree(h->xp);
   cudaFree(h->bias);
   cudaFree(h->scale_inv);
-  cudaFree(h->ws);
-  cudaFree(h->ws_cnt);
   if (h->err_host) cudaFreeHost(const_cast<int32_t*>(h->err_host));
   delete h;
 }
@@ -173,7 +171,7 @@ gptq_status_t gptq_check_shapes(int bits, int64_t qweight_rows, int64_t qweight_
 
 namespace gptq {
 // Argument checks shared by both checkpoint formats, then the handle and its runtime layout.
-static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split);
+static gptq_status_t reserve_impl(Handle& h, int max_M);
 
 static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, const void* scales,
                                  const int32_t* g_idx, int K, int N, int bits, int group_size, gptq_dtype_t dtype,
@@ -223,7 +221,7 @@ static gptq_status_t repack_impl(const void* qweight, const int32_t* qzeros, con
   s = build_runtime(*h, qweight, qzeros, scales, g_idx, fmt, sf32, static_cast<cudaStream_t>(stream));
   if (s != GPTQ_OK) { free_handle(h); return s; }
   h->reserved_M = 0;
-  s = reserve_impl(*h, 32, false);     // the small-M path's permuted-x workspace only
+  s = reserve_impl(*h, 32);     // the permuted-x workspace for M <= 32
   if (s != GPTQ_OK) { free_handle(h); return s; }
   *out = reinterpret_cast<gptq_handle_t>(h);
   return GPTQ_OK;
@@ -284,8 +282,9 @@ gptq_status_t gptq_repack_fp8(const void* weight, const float* scale_inv, int K,
 
 namespace gptq {
 // Workspace for calls with M <= max_M: the permuted-x copy (handles whose sorted order is not the
-// identity) and, when with_split, the large-M kernel's K-split partials and tile counters.
-static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
+// identity).  The K splits of both kernels exchange their partials in shared memory across a
+// thread-block cluster and need none.
+static gptq_status_t reserve_impl(Handle& h, int max_M) {
   if (max_M > h.reserved_M && !h.identity) {
     const size_t bytes = (size_t)max_M * h.Kr * 2;
     void* p = nullptr;
@@ -296,45 +295,6 @@ static gptq_status_t reserve_impl(Handle& h, int max_M, bool with_split) {
     h.xp_bytes = bytes;
   }
   if (max_M > h.reserved_M) h.reserved_M = max_M;
-  if (with_split && max_M > h.split_reserved_M) {
-    size_t need = 0;
-    int need_cnt = 0;
-    for (int M = 1; M <= max_M; ++M) {
-      const int sp = large_split_for(h, M, SIZE_MAX, INT_MAX);
-      if (sp > 1) {
-        need = std::max(need, (size_t)sp * M * h.Np * sizeof(float));
-        need_cnt = std::max(need_cnt, large_tile_count(h, M));
-      }
-    }
-    bool grew = false;
-    if (need > h.ws_bytes) {
-      void* p = nullptr;
-      cudaError_t e = cudaMalloc(&p, need);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(K-split workspace)");
-      cudaFree(h.ws);
-      h.ws = static_cast<float*>(p);
-      h.ws_bytes = need;
-      grew = true;
-    }
-    if (need_cnt > h.ws_cnt_n) {
-      int* p = nullptr;
-      cudaError_t e = cudaMalloc(&p, sizeof(int) * (size_t)need_cnt);
-      if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(int) * (size_t)need_cnt);
-      if (e != cudaSuccess) {
-        cudaFree(p);
-        return cuda_fail(e, "cudaMalloc(K-split counters)");
-      }
-      cudaFree(h.ws_cnt);
-      h.ws_cnt = p;
-      h.ws_cnt_n = need_cnt;
-      grew = true;
-    }
-    if (grew) {   // cached launch plans were made without this workspace
-      std::lock_guard<std::mutex> lock(h.plan_mu);
-      h.plans.clear();
-    }
-    h.split_reserved_M = max_M;
-  }
   return GPTQ_OK;
 }
 }  // namespace gptq
@@ -351,7 +311,7 @@ gptq_status_t gptq_reserve(gptq_handle_t hh, int max_M) {
   if (dev != h.device)
     return fail(GPTQ_ERR_INVALID_ARG, "handle belongs to device " + std::to_string(h.device) + " but device " +
                                           std::to_string(dev) + " is current");
-  return reserve_impl(h, max_M, true);
+  return reserve_impl(h, max_M);
 }
 
 gptq_status_t gptq_gemm(gptq_handle_t h, const void* x, void* y, int M, void* stream) {
@@ -414,8 +374,7 @@ gptq_status_t gptq_get_info(gptq_handle_t hh, gptq_info_t* info) {
   info->weight_bytes = h.wr_bytes();
   info->device_bytes = h.wr_bytes() + sizeof(int32_t) * (size_t)h.Kr + sizeof(int32_t) * (size_t)(h.Kr / 32) +
                        (size_t)h.G * h.Np * (h.fp8 ? 3 : 6) + h.xp_bytes + (h.bias ? sizeof(float) * (size_t)h.Np : 0) +
-                       (h.scale_inv ? sizeof(float) * (size_t)((h.N + 127) / 128) * h.kb : 0) + h.ws_bytes +
-                       sizeof(int) * (size_t)h.ws_cnt_n;
+                       (h.scale_inv ? sizeof(float) * (size_t)((h.N + 127) / 128) * h.kb : 0);
   return GPTQ_OK;
 }
 

@@ -34,8 +34,9 @@
 // FP8 block-scaled layers (template FP8): the dequantisers convert e4m3 pairs (fp8_pair) with no
 // zero, and the scalers multiply by the CTA's 128 x 128 block factor.
 // K split (grids that would leave SMs idle): blockIdx.z takes a range of 128-row blocks, the
-// partials go to an fp32 workspace, and the last CTA of each tile (an atomic counter, no waiting)
-// sums them in range order and stores y.  A very long K narrows the x tile until the tables fit.
+// ranges of a tile form one thread-block cluster, each CTA leaves its fp32 partial in its own
+// shared memory, and CTA z sums the z-th slice of the tile's rows over all ranges in range order
+// (distributed shared memory reads) and stores y.  A very long K narrows the x tile until the tables fit.
 // Every wait is bounded; a timeout sets the handle's error word and the CTA drains and exits.
 #include "internal.cuh"
 
@@ -100,11 +101,9 @@ struct LargeArgs {
   const float* bias;   // [Np] float32 added to y, or nullptr
   const float* scale_inv;   // FP8 layers: [ceil(N/128)][kb] block factors
   int kb;
-  // K split: CTA z of a tile takes 128-row blocks [NB z / split, NB (z + 1) / split); its fp32 partial
-  // goes to ws[z][m][n] and the last CTA of the tile (counted in cnt) sums the partials in z order
+  // K split: CTA z of a tile takes 128-row blocks [NB z / split, NB (z + 1) / split); the tile's
+  // CTAs form one thread-block cluster and sum their fp32 partials in shared memory, in z order
   int split;
-  float* ws;        // [split][M][Np] (split > 1)
-  int* cnt;         // one counter per (m tile, n tile), zero between calls
 };
 
 __device__ __forceinline__ uint32_t and_or_l(uint32_t a, uint32_t b, uint32_t c) {
@@ -234,10 +233,24 @@ __device__ __forceinline__ void reg_after_wait(uint32_t (&r)[16]) {
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                :: "memory");
 }
+// Thread-block cluster helpers (the K split).
+__device__ __forceinline__ void cluster_sync_l() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// 16 bytes of CTA `rank`'s shared memory at the same offset as the local address `smem_addr`.
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t smem_addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(d) : "memory");
+  return v;
+}
+
 template <typename T, int BITS, int BMX, bool FP8>
 __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, const __grid_constant__ CUtensorMap tmap_x) {
   static_assert(BMX == 64 || BMX == 128 || BMX == 256, "MMA N: a multiple of 16 up to 256; TMEM: a power of two");
   static_assert(!FP8 || BITS == 8, "FP8 layers use the 8-bit layout");
+  static_assert((size_t)BMX * BN * 4 <= (size_t)LargeSmem<BITS, BMX>::bars, "K-split partial below the barriers");
   using S = LargeSmem<BITS, BMX>;
   constexpr int XB = X_BYTES<BMX>;
   constexpr int XS = gptq::XS<BITS, BMX>;
@@ -410,71 +423,41 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
     if (!ok) report_timeout(a.err);
     uint16_t* y = static_cast<uint16_t*>(a.y);
     if (a.split > 1) {
-      // this K range's partial, then the tile's counter (every CTA counts once, also after a timeout,
-      // so the counter is back at zero after every call); the CTA that counts last adds the
-      // partials in order of z and stores y.  No CTA waits for another.
-      if (n < a.N) {
+      // This K range's partial goes into the CTA's own shared memory, [x row][weight row] fp32, over
+      // the x ring and what follows it (idle now: every MMA that read them has completed, and every
+      // copy into them was consumed).  The K ranges of a tile are the CTAs of one cluster
+      // (1 x 1 x split).  Once every partial is in place, CTA z sums the z-th slice of the tile's x
+      // rows over all ranges, in order of z (the same sum whichever CTA adds it), reading the other
+      // CTAs' shared memory, and stores y; a second cluster barrier keeps every CTA until no other
+      // still reads its partial.  Every thread of every CTA passes both barriers (the other warps at
+      // the end of their roles), after a timeout too.
+      float* part = reinterpret_cast<float*>(base);
 #pragma unroll
-        for (int j = 0; j < HC; ++j) {
-          const int m = m0 + HC * hs + j;
-          if (m < a.M) a.ws[((size_t)z * a.M + m) * a.Np + n] = acc[j];
+      for (int j = 0; j < HC; ++j) part[(HC * hs + j) * BN + nrow] = acc[j];
+      cluster_sync_l();
+      const int rows = min(BMX, a.M - m0), S = a.split;
+      const int r0 = rows * z / S, r1 = rows * (z + 1) / S;
+      for (int i = 32 * sw + lane; i < (r1 - r0) * (BN / 4); i += 32 * kSc) {
+        const int m = r0 + i / (BN / 4), nn = 4 * (i % (BN / 4));
+        const uint32_t off = base_s + (uint32_t)((m * BN + nn) * 4);
+        float4 t = ld_cluster_f4(off, 0);
+        for (int zz = 1; zz < S; ++zz) {
+          const float4 v = ld_cluster_f4(off, (uint32_t)zz);
+          t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
         }
-      }
-      __threadfence();
-      asm volatile("bar.sync 1, %0;" :: "n"(32 * kSc) : "memory");     // the scaler warps only
-      if (sw == 0 && lane == 0) {
-        const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-        const int before = atomicAdd(&a.cnt[tile], 1);
-        const uint32_t last = before == a.split - 1 ? 1u : 0u;
-        if (last) {
-          atomicExch(&a.cnt[tile], 0);
-          __threadfence();
-        }
-        tmem_slot[1] = last;
-      }
-      asm volatile("bar.sync 1, %0;" :: "n"(32 * kSc) : "memory");
-      if (tmem_slot[1] != 0u) {
-        // the tile's rows as float4 runs of four columns, spread over the scaler threads, every
-        // partial (this CTA's included) read back from L2 in order of z: the same sum whichever CTA
-        // of the tile is last; four runs per thread in flight
-        const int rows = min(BMX, a.M - m0);
-        const int runs = rows * (BN / 4);
-        for (int i0 = 32 * sw + lane; i0 < runs; i0 += 4 * 32 * kSc) {
-          float4 t[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) t[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int zz = 0; zz < a.split; ++zz) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i = i0 + u * 32 * kSc;
-              if (i < runs) {
-                const int m = m0 + i / (BN / 4), nn = n0 + 4 * (i % (BN / 4));
-                if (nn < a.N) {
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws + ((size_t)zz * a.M + m) * a.Np + nn));
-                  t[u].x += v.x; t[u].y += v.y; t[u].z += v.z; t[u].w += v.w;
-                }
-              }
-            }
+        const int gn = n0 + nn;
+        if (gn < a.N) {
+          if (a.bias) {
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(a.bias + gn));
+            t.x += bb.x; t.y += bb.y; t.z += bb.z; t.w += bb.w;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * 32 * kSc;
-            if (i < runs) {
-              const int m = m0 + i / (BN / 4), nn = n0 + 4 * (i % (BN / 4));
-              if (nn < a.N) {
-                if (a.bias) {
-                  const float4 b = __ldg(reinterpret_cast<const float4*>(a.bias + nn));
-                  t[u].x += b.x; t[u].y += b.y; t[u].z += b.z; t[u].w += b.w;
-                }
-                uint2 o;
-                o.x = (uint32_t)to_bits<T>(t[u].x) | ((uint32_t)to_bits<T>(t[u].y) << 16);
-                o.y = (uint32_t)to_bits<T>(t[u].z) | ((uint32_t)to_bits<T>(t[u].w) << 16);
-                *reinterpret_cast<uint2*>(y + (size_t)m * a.N + nn) = o;
-              }
-            }
-          }
+          uint2 o;
+          o.x = (uint32_t)to_bits<T>(t.x) | ((uint32_t)to_bits<T>(t.y) << 16);
+          o.y = (uint32_t)to_bits<T>(t.z) | ((uint32_t)to_bits<T>(t.w) << 16);
+          *reinterpret_cast<uint2*>(y + (size_t)(m0 + m) * a.N + gn) = o;
         }
       }
+      cluster_sync_l();
     } else if (n < a.N) {
       // y[m][n] for the HC x rows of this half: lanes are consecutive n, so each store is 64 bytes
       if (a.bias) {
@@ -638,6 +621,10 @@ __global__ void __launch_bounds__(kThreadsL, 1) k_gemm_large(const LargeArgs a, 
       }
       if (!ok) report_timeout(a.err);
     }
+    if (a.split > 1) {   // the cluster's two barriers around the scalers' reduction of the partials
+      cluster_sync_l();
+      cluster_sync_l();
+    }
   }
 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -684,14 +671,13 @@ inline int large_bmx(const Handle& h, int M) {
 }  // namespace
 
 // K split of the large-M kernel at M: the number of ranges s (1 .. 8, each of at least 8 blocks)
-// with the smallest estimated time waves(s) * (t0 + t_k / s) + t_red(s), where waves(s) =
-// ceil(tiles s / SMs), t_k is one CTA's pass over all of K (~700 / 800 / 950 cycles per 64-k stage
-// at 64 / 128 / 256 x rows, at 1.9 GHz), t0 ~3 us a CTA's fixed start and drain, and t_red the last
-// CTA's read of the s partials of its tile at ~130 GB/s -- a grid with fewer tiles than SMs, or a
-// mostly empty last wave, gains -- and whose partials fit kSplitWsCap bytes.  `avail` and `cnt`
-// (workspace bytes and counters on hand) bound it further; pass SIZE_MAX / INT_MAX to ask what M
-// would take.
-int large_split_for(const Handle& h, int M, size_t avail, int cnt) {
+// with the smallest estimated time waves(s) * (t0 + t_k / s + t_red(s)), where waves(s) =
+// ceil(tiles / clusters of s CTAs that run at once), t_k is one CTA's pass over all of K (~700 / 800
+// / 950 cycles per 64-k stage at 64 / 128 / 256 x rows, at 1.9 GHz), t0 ~3 us a CTA's fixed start
+// and drain, and t_red the cluster's reduction (two cluster barriers, ~0.8 us, and each CTA's read of
+// one slice from every range, ~150 GB/s).  A grid with fewer tiles than SMs, or a mostly empty last
+// wave, gains.  No workspace: the partials stay in the cluster's shared memory.
+int large_split(const Handle& h, int M) {
   const int bmx = M > 0 ? large_bmx(h, M) : 0;
   if (bmx == 0) return 1;
   const long tiles = (long)((M + bmx - 1) / bmx) * (h.Np / BN);
@@ -700,27 +686,20 @@ int large_split_for(const Handle& h, int M, size_t avail, int cnt) {
   const double t_k = (h.Kr / 64) * stage_cycles / 1.9e3;          // us
   const double t0 = 3.0;
   auto cost = [&](int s) {
-    const double waves = (double)((tiles * s + h.sm_count - 1) / h.sm_count);
-    const double red = s > 1 ? (double)s * std::min(M, bmx) * BN * 4 / 130e3 : 0.0;
-    return waves * (t0 + t_k / s) + red;
+    const long slots = s > 1 ? whole_sm_clusters(h, s) : h.sm_count;
+    const double waves = (double)((tiles + slots - 1) / slots);
+    const double red = s > 1 ? 0.8 + (double)std::min(M, bmx) * BN * 4 / 150e3 : 0.0;
+    return waves * (t0 + t_k / s + red);
   };
   int best = 1;
   double best_cost = cost(1);
   for (int s = 2; s <= 8 && nb / s >= 8; ++s) {
-    const size_t bytes = (size_t)s * M * h.Np * sizeof(float);
-    if (cost(s) < best_cost * 0.95 && bytes <= kSplitWsCap && bytes <= avail && tiles <= cnt) {
+    if (cost(s) < best_cost * 0.95) {
       best = s;
       best_cost = cost(s);
     }
   }
   return best;
-}
-
-int large_split(const Handle& h, int M) { return large_split_for(h, M, h.ws_bytes, h.ws_cnt_n); }
-
-int large_tile_count(const Handle& h, int M) {
-  const int bmx = M > 0 ? large_bmx(h, M) : 0;
-  return bmx ? (M + bmx - 1) / bmx * (h.Np / BN) : 0;
 }
 
 namespace {
@@ -741,17 +720,21 @@ cudaError_t launch_tbm(const Handle& h, const CUtensorMap& map, void* y, int M, 
   if (e != cudaSuccess) return e;
   const int split = large_split(h, M);
   LargeArgs args{h.wr, h.cgid, h.s_r, h.z_r, y, h.err, M, h.N, h.Np, h.Kr, h.G, h.zoff, h.has_bias ? h.bias : nullptr,
-                 h.scale_inv, h.kb, split, h.ws, h.ws_cnt};
+                 h.scale_inv, h.kb, split};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + BMX - 1) / BMX, h.Np / BN, split);  // consecutive CTAs share a weight tile
   cfg.blockDim = dim3(kThreadsL);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;   // K split: a tile's ranges form one cluster
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = (unsigned)split;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = split > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, args, map);
 }
 

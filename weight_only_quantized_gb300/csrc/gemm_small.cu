@@ -36,6 +36,9 @@
 //    planner takes 8 consumer warps, smaller K panels and recomputes the x sums for every tile.
 //  * Every wait is bounded; a timeout sets the handle's error word, and the CTA drains its copies
 //    and exits.
+// This file is compiled twice: as itself (fp16 layers, the plan queries and the cluster count) and,
+// through gemm_small_bf16.cu with GPTQ_SMALL_BF16_UNIT, for bf16 layers, so that the two halves of
+// the kernel instantiations build in parallel.
 #include "internal.cuh"
 
 #include <algorithm>
@@ -952,45 +955,6 @@ struct SmallPlan {
       gather, o_pm, o_raw, cg_async, xs_on, split, o_recv;
 };
 
-// This file is compiled twice: as itself (fp16 layers and the plan queries) and, through
-// gemm_small_bf16.cu, for bf16 layers, so that the two halves of the kernel instantiations build in
-// parallel.
-#ifdef GPTQ_SMALL_BF16_UNIT
-using UnitT = __nv_bfloat16;
-#else
-using UnitT = __half;
-#endif
-
-// Clusters of S CTAs that take a whole SM each and that the GPU runs at once.  One kernel built for
-// clusters answers for all of them: at one CTA per SM the count depends only on the cluster size
-// and on how the SMs are grouped.
-int whole_sm_clusters(const Handle& h, int S) {
-  const int idx = S == 2 ? 1 : S == 4 ? 2 : S == 8 ? 3 : 0;
-  if (idx == 0) return h.sm_count;
-  int n = h.clusters_fit[idx].load(std::memory_order_relaxed);
-  if (n > 0) return n;
-  auto fn = k_gemm_small<UnitT, 4, 2, 8, false, false, true, true>;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 1;
-  at[0].val.clusterDim.y = (unsigned)S;
-  at[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1, (unsigned)S);
-  cfg.blockDim = dim3(threads_of<8>());
-  cfg.dynamicSmemBytes = kSmemFull;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemFull) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
-    (void)cudaGetLastError();
-    n = h.sm_count / S;
-  }
-  n = std::max(1, std::min(n, h.sm_count / S));
-  h.clusters_fit[idx].store(n, std::memory_order_relaxed);
-  return n;
-}
-
 // K split for layers with fewer 32-column tiles than SMs (M <= 8): the largest of 2, 4, 8 K panels
 // whose CTAs (one per tile and panel, a whole SM each; a tile's panels form one cluster) all run
 // at once, with at least two stages per panel; 1 = no split.  The split costs about a
@@ -1254,6 +1218,39 @@ cudaError_t launch_dtype(const Handle& h, const void* x, void* y, int M, cudaStr
 }
 
 }  // namespace
+
+#ifndef GPTQ_SMALL_BF16_UNIT
+// Clusters of S CTAs that take a whole SM each and that the GPU runs at once (also used by the
+// large-M kernel's K split: both kernels run one CTA per SM).  One kernel built for clusters answers
+// for all of them: at one CTA per SM the count depends only on the cluster size and on how the SMs
+// are grouped.
+int whole_sm_clusters(const Handle& h, int S) {
+  if (S <= 1 || S > 8) return S == 1 ? h.sm_count : 0;
+  const int idx = S;
+  int n = h.clusters_fit[idx].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  auto fn = k_gemm_small<__half, 4, 2, 8, false, false, true, true>;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = (unsigned)S;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, (unsigned)S);
+  cfg.blockDim = dim3(threads_of<8>());
+  cfg.dynamicSmemBytes = kSmemFull;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemFull) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = h.sm_count / S;
+  }
+  n = std::max(1, std::min(n, h.sm_count / S));
+  h.clusters_fit[idx].store(n, std::memory_order_relaxed);
+  return n;
+}
+#endif
 
 #ifndef GPTQ_SMALL_BF16_UNIT
 int small_m_max() { return 32; }

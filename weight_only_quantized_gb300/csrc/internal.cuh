@@ -35,12 +35,6 @@ struct Handle {
   uint8_t* z_r = nullptr;    // [G][Np] stored zero field (GPTQ: zero - 1; AWQ: the zero itself)
   int zoff = 1;              // zero = stored field + zoff: 1 for GPTQ v1 fields, 0 for gptq_v2 and AWQ
   float* bias = nullptr;     // [Np] float32 bias added to y (pad columns 0), allocated by gptq_set_bias
-  // K-split workspace of the large-M kernel (sized by gptq_reserve)
-  float* ws = nullptr;       // fp32 partials [split][M][Np]
-  size_t ws_bytes = 0;
-  int* ws_cnt = nullptr;     // one counter per (m tile, n tile), zero between calls
-  int ws_cnt_n = 0;
-  int split_reserved_M = 0;  // gptq_reserve sized the split workspace for M up to this
   // FP8 block-scaled layers (codes are e4m3 bytes; no zeros; s_r and z_r are not allocated)
   int fp8 = 0;
   float* scale_inv = nullptr;   // [ceil(N/128)][kb] float32, one factor per 128 x 128 block
@@ -68,10 +62,10 @@ struct Handle {
   // Launch plans by (path, M): computed once, so a call costs one kernel launch on the host.
   mutable std::mutex plan_mu;
   mutable std::unordered_map<int64_t, std::vector<int64_t>> plans;
-  // Thread-block clusters of 2, 4 and 8 whole-SM CTAs that the GPU holds at once (index log2 of
-  // the size; 0: not queried yet).  The SMs pair up by TPC and group by GPC, so a cluster size
-  // that does not divide a GPC's SMs leaves some of them idle.
-  mutable std::atomic<int> clusters_fit[4] = {0, 0, 0, 0};
+  // Thread-block clusters of S = 2 .. 8 whole-SM CTAs that the GPU holds at once (index S; 0: not
+  // queried yet).  The SMs pair up by TPC and group by GPC, so a cluster size that does not divide
+  // a GPC's SMs leaves some of them idle.
+  mutable std::atomic<int> clusters_fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 
 // 128-row blocks fetched by one TMA box of the small-M kernel.
@@ -126,10 +120,9 @@ cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst
 
 // Large-M K split: ranges for M given the workspace on hand (1 = none); the workspace bytes a split
 // may take at most.
-constexpr size_t kSplitWsCap = 64ull << 20;
-int large_split_for(const Handle& h, int M, size_t avail, int cnt);
 int large_split(const Handle& h, int M);
-int large_tile_count(const Handle& h, int M);   // output tiles (x tile x 128 weight rows) at M
+// Thread-block clusters of S CTAs with a whole SM each that the GPU runs at once (S = 1, 2, 4, 8).
+int whole_sm_clusters(const Handle& h, int S);
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
 int small_m_launches(const Handle& h, int M);
