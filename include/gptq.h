@@ -334,6 +334,9 @@ typedef struct {
   int k_splits;        /* CTAs that share one output tile's K (1 = no split)                    */
   int k_panels;        /* small-M: K panels x is staged in (1 = all of K at once)               */
   int stages;          /* weight ring depth                                                     */
+  int row_passes;      /* small-M: 2 when the call runs as two launches over row slices of x and
+                          y (the first 16 rows, then the rest), 1 otherwise; the fields above then
+                          describe the first pass, and `launches` counts both                  */
 } gptq_plan_t;
 
 /* Errors: INVALID_ARG (bad handle, M < 1, unknown path, M above the small-M kernel's 32 rows),

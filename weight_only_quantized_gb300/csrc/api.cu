@@ -20,7 +20,8 @@ constexpr int kMaxGroups = GPTQ_MAX_GROUPS;
 // the layer is HBM-bound on GB300 (ridge M* = P * 4.125 / (16 * BW) ~ 72 for 4-bit group 128) and
 // the swap-AB mma.sync kernel keeps every SM streaming weights.  With four m-tiles it also beats
 // the tcgen05 kernel up to M = 28 (measured: 22 vs 28 us at M = 24 on a 4096 x 14336 layer, 84 vs
-// 110 us on 8192 x 28672); above that its x panels shrink to four blocks and it falls behind.
+// 110 us on 8192 x 28672); above that its x panels shrink to four blocks and it falls behind, unless
+// the call runs as two passes of at most 16 rows (auto_path).
 constexpr int kSmallMMax = 28;
 }  // namespace
 
@@ -70,6 +71,43 @@ static gptq_status_t check_device(int* dev_out, int* sms_out) {
   return GPTQ_OK;
 }
 
+// Rows of the first of the small-M kernel's passes at M (M when the call is one pass).  At M = 17 .. 32
+// the kernel stages x per K panel when x of M rows over all of K does not fit its shared memory.
+// With four or more panels, on a layer with at least one 32-column tile per SM, two launches over
+// row slices -- the first 16 rows (two m-tiles: x staged once, or split across a cluster), then
+// the rest -- take less time: 70B gate layer M = 24 104.1 -> 74.7 us, M = 28 111.7 -> 90.7 us;
+// decode layer M = 28 28.6 -> 22.6 us.  With fewer tiles than SMs the second launch's fixed cost
+// wins (K = N = 4096, 8-bit, M = 28: 14.8 vs 18.7 us), and at three panels neither does (decode
+// layer M = 17: 20.3 vs 25.6 us).  Every row's result is its own sum either way, within the same
+// tolerance; the summation order differs between the plans.
+static int small_first_rows(const Handle& h, int M) {
+  if (M <= 16 || M > small_m_max()) return M;
+  const int64_t key = ((int64_t)0x7f << 32) | (uint32_t)M;   // cached beside the launch plans
+  {
+    std::lock_guard<std::mutex> lock(h.plan_mu);
+    auto it = h.plans.find(key);
+    if (it != h.plans.end()) return (int)it->second[0];
+  }
+  gptq_plan_t p{};
+  const int m1 = (small_m_plan_info(h, M, &p) && p.k_panels >= 4 && (h.N + 31) / 32 >= h.sm_count) ? 16 : M;
+  std::lock_guard<std::mutex> lock(h.plan_mu);
+  h.plans[key] = std::vector<int64_t>{m1};
+  return m1;
+}
+
+// GPTQ_PATH_AUTO: the small-M kernel up to kSmallMMax rows, and up to its 32 rows where it runs as
+// two passes (70B gate layer M = 32: 91 us in two passes against 95.7 us on the large-M kernel;
+// decode layer: ~22.8 against 29.2 us); the large-M kernel above.
+static gptq_path_t auto_path(const Handle& h, int M) {
+  if (!large_m_available() || M <= kSmallMMax) return GPTQ_PATH_SMALL_M;
+  return (M <= small_m_max() && small_first_rows(h, M) < M) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+}
+
+static int small_launches_total(const Handle& h, int M) {
+  const int m1 = small_first_rows(h, M);
+  return small_m_launches(h, m1) + (m1 < M ? small_m_launches(h, M - m1) : 0);
+}
+
 static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, gptq_path_t path, void* stream) {
   if (!hh) return fail(GPTQ_ERR_INVALID_ARG, "handle is NULL");
   const Handle& h = *reinterpret_cast<const Handle*>(hh);
@@ -93,7 +131,7 @@ static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, 
   if (*h.err_host != DEV_ERR_NONE)
     return fail(GPTQ_ERR_TIMEOUT, "an earlier call on this handle gave up a bounded device-side wait and its output "
                                   "was invalid; gptq_device_status clears the record");
-  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  if (path == GPTQ_PATH_AUTO) path = auto_path(h, M);
   if (path == GPTQ_PATH_LARGE_M && !large_m_available())
     return fail(GPTQ_ERR_UNSUPPORTED, "the large-M kernel is not part of this build");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -106,10 +144,16 @@ static gptq_status_t gemm_impl(gptq_handle_t hh, const void* x, void* y, int M, 
     if (M > small_m_max())
       return fail(GPTQ_ERR_INVALID_ARG, "M = " + std::to_string(M) + " is above the small-M kernel's " +
                                             std::to_string(small_m_max()) + " rows");
-    if (!h.identity && M > h.reserved_M && small_m_launches(h, M) == 2)
-      return fail(GPTQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs gptq_reserve(h, M): the handle's g_idx "
-                                      "order is not the identity and only M <= " + std::to_string(h.reserved_M) + " is reserved");
-    e = launch_gemm_small(h, x, y, M, st);
+    const int m1 = small_first_rows(h, M);
+    // a pass that gathers x into the workspace needs its rows reserved
+    for (const int r : {m1, M - m1})
+      if (r > 0 && !h.identity && r > h.reserved_M && small_m_launches(h, r) == 2)
+        return fail(GPTQ_ERR_WORKSPACE, "M = " + std::to_string(M) + " needs gptq_reserve(h, " + std::to_string(r) +
+                                        "): the handle's g_idx order is not the identity and only M <= " +
+                                        std::to_string(h.reserved_M) + " is reserved");
+    e = launch_gemm_small(h, x, y, m1, st);
+    if (e == cudaSuccess && m1 < M)
+      e = launch_gemm_small(h, xb + (size_t)m1 * h.K * es, static_cast<char*>(y) + (size_t)m1 * h.N * es, M - m1, st);
   }
   if (e != cudaSuccess) return cuda_fail(e, "gptq_gemm launch");
   return GPTQ_OK;
@@ -326,16 +370,16 @@ int gptq_gemm_launches(gptq_handle_t hh, int M, gptq_path_t path) {
   if (!hh || M < 0) return -1;
   const Handle& h = *reinterpret_cast<const Handle*>(hh);
   if (M == 0) return 0;
-  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
-  return path == GPTQ_PATH_LARGE_M ? large_m_launches(h, M) : small_m_launches(h, M);
+  if (path == GPTQ_PATH_AUTO) path = auto_path(h, M);
+  return path == GPTQ_PATH_LARGE_M ? large_m_launches(h, M) : small_launches_total(h, M);
 }
 
 int gptq_gemm_k_splits(gptq_handle_t hh, int M, gptq_path_t path) {
   if (!hh || M < 0) return -1;
   if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M) return -1;
   const Handle& h = *reinterpret_cast<const Handle*>(hh);
-  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
-  return path == GPTQ_PATH_LARGE_M ? large_split(h, M) : small_m_k_splits(h, M);
+  if (path == GPTQ_PATH_AUTO) path = auto_path(h, M);
+  return path == GPTQ_PATH_LARGE_M ? large_split(h, M) : small_m_k_splits(h, small_first_rows(h, M));
 }
 
 gptq_status_t gptq_destroy(gptq_handle_t hh) {
@@ -407,16 +451,21 @@ gptq_status_t gptq_gemm_plan(gptq_handle_t hh, int M, gptq_path_t path, gptq_pla
   if (path != GPTQ_PATH_AUTO && path != GPTQ_PATH_SMALL_M && path != GPTQ_PATH_LARGE_M)
     return fail(GPTQ_ERR_INVALID_ARG, "unknown path");
   const Handle& h = *reinterpret_cast<const Handle*>(hh);
-  if (path == GPTQ_PATH_AUTO) path = (M <= kSmallMMax || !large_m_available()) ? GPTQ_PATH_SMALL_M : GPTQ_PATH_LARGE_M;
+  if (path == GPTQ_PATH_AUTO) path = auto_path(h, M);
   std::memset(plan, 0, sizeof(*plan));
   plan->path = path;
   if (path == GPTQ_PATH_SMALL_M) {
     if (M > small_m_max())
       return fail(GPTQ_ERR_INVALID_ARG, "M = " + std::to_string(M) + " is above the small-M kernel's " +
                                             std::to_string(small_m_max()) + " rows");
-    if (!small_m_plan_info(h, M, plan)) return fail(GPTQ_ERR_UNSUPPORTED, "no small-M plan fits this layer");
+    const int m1 = small_first_rows(h, M);
+    if (!small_m_plan_info(h, m1, plan)) return fail(GPTQ_ERR_UNSUPPORTED, "no small-M plan fits this layer");
+    plan->launches = small_launches_total(h, M);
+    plan->row_passes = m1 < M ? 2 : 1;
   } else if (!large_m_plan_info(h, M, plan)) {
     return fail(GPTQ_ERR_UNSUPPORTED, "no large-M plan fits this layer");
+  } else {
+    plan->row_passes = 1;
   }
   return GPTQ_OK;
 }

@@ -42,7 +42,7 @@ class GptqPlan(C.Structure):
     _fields_ = [("path", C.c_int), ("launches", C.c_int), ("grid", C.c_int), ("threads", C.c_int),
                 ("smem_bytes", C.c_int), ("consumer_warps", C.c_int), ("m_tiles", C.c_int),
                 ("act_order_in_kernel", C.c_int), ("k_splits", C.c_int), ("k_panels", C.c_int),
-                ("stages", C.c_int)]
+                ("stages", C.c_int), ("row_passes", C.c_int)]
 
 
 SIGNATURES = {
