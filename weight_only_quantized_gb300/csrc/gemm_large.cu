@@ -694,6 +694,7 @@ int large_split(const Handle& h, int M) {
   int best = 1;
   double best_cost = cost(1);
   for (int s = 2; s <= 8 && nb / s >= 8; ++s) {
+    if (whole_sm_clusters(h, s) < 1) continue;   // no cluster of s CTAs fits the GPU
     if (cost(s) < best_cost * 0.95) {
       best = s;
       best_cost = cost(s);

@@ -1000,6 +1000,7 @@ bool plan_layout(const Handle& h, int M, int bits, int mt8, bool with_gather, Sm
   const int NB = h.Kr / 128;
   p.ntiles = (h.N + kTileN - 1) / kTileN;
   p.grid = split > 1 ? std::min(p.ntiles, whole_sm_clusters(h, split)) : std::min(p.ntiles, h.sm_count);
+  if (p.grid < 1) return false;   // no cluster of this size fits the GPU
   p.split = split;
   const int pb_split = ((NB + split - 1) / split + kSPB - 1) / kSPB * kSPB;
   // K-panel: all of K when x fits, else as many blocks as kXPanel holds (x double buffered)
@@ -1228,7 +1229,7 @@ int whole_sm_clusters(const Handle& h, int S) {
   if (S <= 1 || S > 8) return S == 1 ? h.sm_count : 0;
   const int idx = S;
   int n = h.clusters_fit[idx].load(std::memory_order_relaxed);
-  if (n > 0) return n;
+  if (n != 0) return n > 0 ? n : 0;   // -1: queried, none fit
   auto fn = k_gemm_small<__half, 4, 2, 8, false, false, true, true>;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1242,12 +1243,12 @@ int whole_sm_clusters(const Handle& h, int S) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemFull) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
-    n = h.sm_count / S;
+    n = 0;   // unknown: no split of this size is planned
   }
-  n = std::max(1, std::min(n, h.sm_count / S));
-  h.clusters_fit[idx].store(n, std::memory_order_relaxed);
+  n = std::max(0, std::min(n, h.sm_count / S));
+  h.clusters_fit[idx].store(n > 0 ? n : -1, std::memory_order_relaxed);
   return n;
 }
 #endif

@@ -63,8 +63,8 @@ struct Handle {
   mutable std::mutex plan_mu;
   mutable std::unordered_map<int64_t, std::vector<int64_t>> plans;
   // Thread-block clusters of S = 2 .. 8 whole-SM CTAs that the GPU holds at once (index S; 0: not
-  // queried yet).  The SMs pair up by TPC and group by GPC, so a cluster size that does not divide
-  // a GPC's SMs leaves some of them idle.
+  // queried yet, -1: none).  The SMs pair up by TPC and group by GPC, so a cluster size that does
+  // not divide a GPC's SMs leaves some of them idle.
   mutable std::atomic<int> clusters_fit[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 
@@ -121,7 +121,8 @@ cudaError_t launch_bias_f32(const void* src, int kind, int N, int Np, float* dst
 // Large-M K split: ranges for M given the workspace on hand (1 = none); the workspace bytes a split
 // may take at most.
 int large_split(const Handle& h, int M);
-// Thread-block clusters of S CTAs with a whole SM each that the GPU runs at once (S = 1, 2, 4, 8).
+// Thread-block clusters of S CTAs with a whole SM each that the GPU runs at once (S = 1 .. 8); 0 when
+// none fits, or the query failed (no split of that size is then planned).
 int whole_sm_clusters(const Handle& h, int S);
 
 // Small-M path: persistent bulk-copy-fed mma.sync (swap-AB) kernel (plus an x gather when not identity).
