@@ -34,6 +34,11 @@
 //    no zero fold, and the 128 x 128 block's factor multiplies the partial sum.
 //  * Very long K (template XS false): when the per-block x-sum table does not fit shared memory the
 //    planner takes 8 consumer warps, smaller K panels and recomputes the x sums for every tile.
+//  * K split (template SPLIT), for layers with fewer 32-column tiles than SMs at M <= 8 and for
+//    layers whose x over all of K does not fit shared memory at M = 9 .. 16: the CTAs of a
+//    thread-block cluster take the K panels of a tile (or of a run of tiles), each stages x of its
+//    panel once, and the first CTA adds up the others' tile sums, sent into its shared memory by
+//    st.async.
 //  * Every wait is bounded; a timeout sets the handle's error word, and the CTA drains its copies
 //    and exits.
 // This file is compiled twice: as itself (fp16 layers, the plan queries and the cluster count) and,
