@@ -88,3 +88,23 @@ def test_auto_takes_two_passes_up_to_32_rows():
     compare(run_gemm(h, x, spec.N, gptq.PATH_AUTO), oracle_y(ck, x))
     h2 = repack(synth.make_checkpoint(synth.LayerSpec(4096, 4096, 4, 128, False, True, "bf16"), seed=13))
     assert gptq.gptq_gemm_plan(h2, 30, gptq.PATH_AUTO).path == gptq.PATH_LARGE_M   # fewer tiles than SMs
+
+
+def test_two_passes_with_bias_awq_and_fp8():
+    """The second pass writes y at a row offset and adds the bias again: AWQ with a bias, and an FP8
+    block-scaled layer, both at M = 28 in two passes."""
+    import oracle
+    K, N = 4096, 5120
+    b = torch.randn(N, generator=torch.Generator().manual_seed(21)) * 0.1
+    ck = synth.make_awq_checkpoint(K, N, 128, "fp16", seed=22)
+    h = gptq.gptq_repack_awq(ck.qweight.cuda(), ck.qzeros.cuda(), ck.scales.cuda(), 128)
+    gptq.gptq_set_bias(h, b.half().cuda())
+    assert gptq.gptq_gemm_plan(h, 28, gptq.PATH_SMALL_M).row_passes == 2
+    x = synth.make_x(28, K, "fp16", seed=23)
+    y_ref = oracle.awq_linear(ck.qweight, ck.qzeros, ck.scales, 128, "fp16", x) + b.half().double().numpy()[None, :]
+    compare(run_gemm(h, x, N, gptq.PATH_SMALL_M), y_ref)
+    f8 = synth.make_fp8_checkpoint(K, N, "bf16", seed=24)
+    h8 = gptq.gptq_repack_fp8(f8.weight.cuda(), f8.scale_inv.cuda(), torch.bfloat16)
+    assert gptq.gptq_gemm_plan(h8, 28, gptq.PATH_AUTO).row_passes == 2
+    x8 = synth.make_x(28, K, "bf16", seed=25)
+    compare(run_gemm(h8, x8, N, gptq.PATH_AUTO), oracle.fp8_linear(f8.weight, f8.scale_inv, "bf16", x8))
