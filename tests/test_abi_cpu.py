@@ -156,3 +156,30 @@ def test_limits_shared_by_header_and_library():
     args = [dummy, dummy, dummy, None, 131072 + 32, 256, 4, 128, 0, dummy, C.c_size_t(1 << 40), dummy, dummy,
             1 << 20, dummy, dummy, C.byref(kr), None]
     assert L.gptq_repack_noalloc(*args) == 2
+
+
+def _c_layout(struct, fields):
+    """sizeof and offsetof of a header struct, from a C program compiled against include/gptq.h."""
+    import subprocess
+    import tempfile
+    body = "\n".join(f'  printf("{f} %zu\\n", offsetof({struct}, {f}));' for f in fields)
+    src = (f'#include <stdio.h>\n#include <stddef.h>\n#include "gptq.h"\n'
+           f'int main(void) {{\n  printf("sizeof %zu\\n", sizeof({struct}));\n{body}\n  return 0;\n}}\n')
+    with tempfile.TemporaryDirectory() as d:
+        c, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True,
+                       capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    return {k: int(v) for k, v in (line.split() for line in out.splitlines())}
+
+
+@pytest.mark.parametrize("struct,cls", [("gptq_plan_t", gptq.GptqPlan), ("gptq_info_t", gptq.GptqInfo)])
+def test_binding_structs_match_the_header(struct, cls):
+    """The ctypes mirrors in the binding have the header's size and field offsets, so a field added
+    on one side only is caught without a GPU."""
+    fields = [f for f, _ in cls._fields_]
+    lay = _c_layout(struct, fields)
+    assert lay["sizeof"] == C.sizeof(cls)
+    for f in fields:
+        assert lay[f] == getattr(cls, f).offset, f
